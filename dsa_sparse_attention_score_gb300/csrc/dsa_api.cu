@@ -1,0 +1,363 @@
+// dsa_api.cu -- the C ABI declared in include/dsa.h: argument validation,
+// workspace layout, TMA tensor maps and the launch order of each call.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+using namespace dsa;
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr size_t kAlign = 256;
+constexpr int64_t kSlabBytes = int64_t(1) << 30;  // score slab budget in the workspace
+constexpr int kSMs = 152;
+
+cudaEvent_t *g_trace = nullptr;
+int g_trace_n = 0;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+dsa_status_t check_batch(const dsa_batch_t *b) {
+    if (!b) return DSA_ERR_INVALID_ARGUMENT;
+    if (b->batch < 1 || b->total_q < 1 || b->max_q_per_seq < 1 || b->max_kv < 1 || b->cache_rows < 1)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (b->cache_rows > INT32_MAX || (int64_t)b->batch * b->max_q_per_seq < b->total_q)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (!b->cu_q || !b->q_pos || !b->kv_off) return DSA_ERR_INVALID_ARGUMENT;
+    return DSA_OK;
+}
+
+DevBatch dev_batch(const dsa_batch_t *b) {
+    DevBatch d;
+    d.B = b->batch;
+    d.T = b->total_q;
+    d.max_q = b->max_q_per_seq;
+    d.max_kv = b->max_kv;
+    d.cache_rows = b->cache_rows;
+    d.cu_q = b->cu_q;
+    d.q_pos = b->q_pos;
+    d.kv_off = b->kv_off;
+    return d;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [rows, cols] of 16-bit elements, SWIZZLE_128B boxes.
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t cols, uint64_t rows,
+              uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- workspace
+struct Layout {
+    size_t status = 0;
+    size_t scores = 0, scores_bytes = 0;
+    size_t idx = 0, idx_bytes = 0;
+    size_t part_o = 0, part_o_bytes = 0;
+    size_t part_ml = 0, part_ml_bytes = 0;
+    size_t total = 0;
+    int J = 0;            // slab window (local tokens per sequence)
+    int64_t ld = 0;       // slab row stride (floats)
+    int n_split = 1, tiles_per_cta = 1;
+};
+
+void attn_split(int T, int k, int *n_split, int *tpc) {
+    const int n_tiles = (k + 127) / 128;
+    int ns = 1;
+    if (T < 2 * kSMs) ns = std::min(n_tiles, (2 * kSMs + T - 1) / T);
+    int t = (n_tiles + ns - 1) / ns;
+    ns = (n_tiles + t - 1) / t;
+    *n_split = ns;
+    *tpc = t;
+}
+
+Layout layout(int op, const dsa_batch_t *b, int k) {
+    Layout L;
+    size_t off = kStatusBytes;
+    if (op == DSA_OP_DECODE) {
+        L.ld = (int64_t)align_up((size_t)b->max_kv, 4);
+        const int64_t row_bytes = L.ld * 4;
+        int64_t J = std::max<int64_t>(1, kSlabBytes / (row_bytes * b->batch));
+        L.J = (int)std::min<int64_t>(J, b->max_q_per_seq);
+        L.scores = off;
+        L.scores_bytes = (size_t)b->batch * L.J * row_bytes;
+        off = align_up(off + L.scores_bytes, kAlign);
+        L.idx = off;
+        L.idx_bytes = (size_t)b->total_q * k * 4;
+        off = align_up(off + L.idx_bytes, kAlign);
+    }
+    if (op == DSA_OP_DECODE || op == DSA_OP_SPARSE_ATTN) {
+        attn_split(b->total_q, k, &L.n_split, &L.tiles_per_cta);
+        if (L.n_split > 1) {
+            L.part_o = off;
+            L.part_o_bytes = (size_t)b->total_q * L.n_split * 64 * D_L * 4;
+            off = align_up(off + L.part_o_bytes, kAlign);
+            L.part_ml = off;
+            L.part_ml_bytes = (size_t)b->total_q * L.n_split * 64 * 2 * 4;
+            off = align_up(off + L.part_ml_bytes, kAlign);
+        }
+    }
+    L.total = off;
+    return L;
+}
+
+inline uint32_t *status_ptr(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
+
+dsa_status_t check_ws(void *ws, size_t ws_bytes, size_t need) {
+    if (!ws) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(ws, kAlign)) return DSA_ERR_MISALIGNED;
+    if (ws_bytes < need) return DSA_ERR_WORKSPACE_TOO_SMALL;
+    return DSA_OK;
+}
+
+inline void trace(int i, cudaStream_t s) {
+    if (g_trace && i < g_trace_n && g_trace[i]) cudaEventRecord(g_trace[i], s);
+}
+
+#define DSA_TRY_CUDA(x)                      \
+    do {                                     \
+        if ((x) != cudaSuccess) return DSA_ERR_CUDA; \
+    } while (0)
+
+dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const dsa_bf16 *kv_cache,
+                           const dsa_batch_t *batch, const int32_t *idx, int k, int H, float sm_scale,
+                           float *out, float *lse, void *ws, const Layout &L, cudaStream_t stream,
+                           bool traced) {
+    const DevBatch db = dev_batch(batch);
+    CUtensorMap ql, qr, kv;
+    const uint64_t qrows = (uint64_t)batch->total_q * H;
+    if (!make_map(&ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_lat, D_L, qrows, 64, 64) ||
+        !make_map(&qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_rope, D_R, qrows, 64, 64) ||
+        !make_map(&kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv_cache, D_ROW, (uint64_t)batch->cache_rows, 64, 1))
+        return DSA_ERR_CUDA;
+    AttnLaunch a{};
+    a.H = H;
+    a.k = k;
+    a.sm_scale = sm_scale;
+    a.idx = idx;
+    a.out = out;
+    a.lse = lse;
+    a.n_split = L.n_split;
+    a.tiles_per_cta = L.tiles_per_cta;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    a.part_o = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_o) : nullptr;
+    a.part_ml = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_ml) : nullptr;
+    DSA_TRY_CUDA(launch_sparse_attn(a, ql, qr, kv, db, status_ptr(ws), stream));
+    if (traced) trace(4, stream);
+    DSA_TRY_CUDA(launch_attn_combine(a, db, stream));
+    return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dsa_status_string(dsa_status_t s) {
+    switch (s) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported dimension";
+        case DSA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case DSA_ERR_CUDA: return "CUDA error";
+        case DSA_ERR_DEVICE: return "device reported an error in the status word";
+    }
+    return "unknown status";
+}
+
+int dsa_version(void) { return kVersion; }
+
+dsa_status_t dsa_set_trace_events(cudaEvent_t *events, int n) {
+    if (n < 0) return DSA_ERR_INVALID_ARGUMENT;
+    g_trace = (n > 0) ? events : nullptr;
+    g_trace_n = (events && n > 0) ? n : 0;
+    return DSA_OK;
+}
+
+dsa_status_t dsa_workspace_size(int op, const dsa_batch_t *batch, int H_I, int H, int k, size_t *bytes) {
+    (void)H_I;
+    (void)H;
+    if (!bytes || op < DSA_OP_K_APPEND || op > DSA_OP_DECODE) return DSA_ERR_INVALID_ARGUMENT;
+    if (!batch || batch->batch < 1 || batch->total_q < 1 || batch->max_q_per_seq < 1 || batch->max_kv < 1)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if ((op == DSA_OP_TOPK || op == DSA_OP_SPARSE_ATTN || op == DSA_OP_DECODE) && (k < 1 || k > 65536))
+        return DSA_ERR_UNSUPPORTED;
+    *bytes = layout(op, batch, k).total;
+    return DSA_OK;
+}
+
+dsa_status_t dsa_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes);
+    if (s != DSA_OK) return s;
+    DSA_TRY_CUDA(cudaMemsetAsync(ws, 0, kStatusBytes, stream));
+    return DSA_OK;
+}
+
+dsa_status_t dsa_read_device_status(void *ws, cudaStream_t stream, uint32_t *flags) {
+    if (!ws || !flags) return DSA_ERR_INVALID_ARGUMENT;
+    uint32_t v = 0;
+    DSA_TRY_CUDA(cudaStreamSynchronize(stream));
+    DSA_TRY_CUDA(cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost));
+    DSA_TRY_CUDA(cudaMemset(ws, 0, sizeof v));
+    *flags = v;
+    return v ? DSA_ERR_DEVICE : DSA_OK;
+}
+
+dsa_status_t dsa_indexer_k_append(const void *k_new, int k_dtype, const dsa_batch_t *batch,
+                                  dsa_f16 *k_cache, int hadamard, void *ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!k_new || !k_cache || (k_dtype != DSA_KEY_F32 && k_dtype != DSA_KEY_F16))
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_new, 16) || !aligned(k_cache, 16)) return DSA_ERR_MISALIGNED;
+    if ((s = check_ws(ws, ws_bytes, kStatusBytes)) != DSA_OK) return s;
+    DSA_TRY_CUDA(launch_k_append(k_new, k_dtype, dev_batch(batch), k_cache, hadamard != 0,
+                                 status_ptr(ws), stream));
+    return DSA_OK;
+}
+
+dsa_status_t dsa_indexer_score(const dsa_f16 *q_idx, const float *w, const dsa_f16 *k_cache,
+                               const dsa_batch_t *batch, int H_I, int hadamard_q, float *scores,
+                               int64_t ld_scores, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!q_idx || !w || !k_cache || !scores) return DSA_ERR_INVALID_ARGUMENT;
+    if (H_I < 1 || H_I > 64) return DSA_ERR_UNSUPPORTED;
+    if (ld_scores < batch->max_kv) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_cache, 16) || !aligned(q_idx, 16) || !aligned(w, 4) || !aligned(scores, 4))
+        return DSA_ERR_MISALIGNED;
+    if ((s = check_ws(ws, ws_bytes, kStatusBytes)) != DSA_OK) return s;
+    CUtensorMap km;
+    if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_cache, D_I, (uint64_t)batch->cache_rows, 64, 128))
+        return DSA_ERR_CUDA;
+    ScoreLaunch a{};
+    a.q_idx = q_idx;
+    a.w = w;
+    a.H_I = H_I;
+    a.hadamard_q = hadamard_q != 0;
+    a.scores = scores;
+    a.ld = ld_scores;
+    a.fill_masked = 1;
+    a.rows = RowMap{0, 0, batch->max_q_per_seq};
+    DSA_TRY_CUDA(launch_score(a, km, dev_batch(batch), status_ptr(ws), stream));
+    return DSA_OK;
+}
+
+dsa_status_t dsa_topk(const float *scores, int64_t ld_scores, const dsa_batch_t *batch, int k,
+                      int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!scores || !idx) return DSA_ERR_INVALID_ARGUMENT;
+    if (k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    if (ld_scores < batch->max_kv) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(scores, 4) || !aligned(idx, 4)) return DSA_ERR_MISALIGNED;
+    if ((s = check_ws(ws, ws_bytes, kStatusBytes)) != DSA_OK) return s;
+    DSA_TRY_CUDA(launch_topk(scores, ld_scores, dev_batch(batch), RowMap{0, 0, 1}, k, idx,
+                             status_ptr(ws), stream));
+    return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const dsa_bf16 *kv_cache,
+                                 const dsa_batch_t *batch, const int32_t *idx, int k, int H,
+                                 float sm_scale, float *out, float *lse, void *ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!q_lat || !q_rope || !kv_cache || !idx || !out) return DSA_ERR_INVALID_ARGUMENT;
+    if (H < 1 || H > 64 || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    if ((int64_t)batch->total_q * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+        !aligned(idx, 4) || (lse && !aligned(lse, 4)))
+        return DSA_ERR_MISALIGNED;
+    const Layout L = layout(DSA_OP_SPARSE_ATTN, batch, k);
+    if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
+    return run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream,
+                         false);
+}
+
+dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                        const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
+                        const dsa_bf16 *kv_cache, const dsa_batch_t *batch, int H_I, int H, int k,
+                        float sm_scale, int hadamard, float *out, float *lse, int32_t *idx_out, void *ws,
+                        size_t ws_bytes, cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!k_new || !q_idx || !w || !q_lat || !q_rope || !k_cache || !kv_cache || !out)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (k_dtype != DSA_KEY_F32 && k_dtype != DSA_KEY_F16) return DSA_ERR_INVALID_ARGUMENT;
+    if (H_I < 1 || H_I > 64 || H < 1 || H > 64 || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    if ((int64_t)batch->total_q * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    if (!aligned(k_new, 16) || !aligned(q_idx, 16) || !aligned(w, 4) || !aligned(q_lat, 16) ||
+        !aligned(q_rope, 16) || !aligned(k_cache, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)) || (idx_out && !aligned(idx_out, 4)))
+        return DSA_ERR_MISALIGNED;
+    const Layout L = layout(DSA_OP_DECODE, batch, k);
+    if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
+
+    const DevBatch db = dev_batch(batch);
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    uint32_t *st = status_ptr(ws);
+    float *slab = reinterpret_cast<float *>(w8 + L.scores);
+    int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(w8 + L.idx);
+    CUtensorMap km;
+    if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_cache, D_I, (uint64_t)batch->cache_rows, 64, 128))
+        return DSA_ERR_CUDA;
+
+    trace(0, stream);
+    DSA_TRY_CUDA(launch_k_append(k_new, k_dtype, db, k_cache, hadamard != 0, st, stream));
+    for (int j0 = 0; j0 < batch->max_q_per_seq; j0 += L.J) {
+        ScoreLaunch a{};
+        a.q_idx = q_idx;
+        a.w = w;
+        a.H_I = H_I;
+        a.hadamard_q = hadamard != 0;
+        a.scores = slab;
+        a.ld = L.ld;
+        a.fill_masked = 0;
+        a.rows = RowMap{1, j0, L.J};
+        if (j0 == 0) trace(1, stream);
+        DSA_TRY_CUDA(launch_score(a, km, db, st, stream));
+        if (j0 == 0) trace(2, stream);
+        DSA_TRY_CUDA(launch_topk(slab, L.ld, db, a.rows, k, idx, st, stream));
+    }
+    trace(3, stream);
+    s = run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream, true);
+    if (L.n_split <= 1) trace(4, stream);
+    trace(5, stream);
+    return s;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// dsa_internal.h -- launchers shared between the kernel translation units and
+// the C-ABI host layer.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+struct DevBatch {
+    int B, T;
+    int max_q, max_kv;
+    int64_t cache_rows;
+    const int32_t *cu_q;
+    const int32_t *q_pos;
+    const int64_t *kv_off;
+};
+
+// Rows of a score/top-k slab: either one row per token (direct) or the rows
+// (b, j - j0) of the local-token window [j0, j0 + J) of every sequence.
+struct RowMap {
+    int slab;     // 0 = direct (row = t), 1 = windowed
+    int j0, J;
+};
+
+cudaError_t launch_k_append(const void *k_new, int k_dtype, const DevBatch &b, uint16_t *k_cache,
+                            int hadamard, uint32_t *status, cudaStream_t stream);
+
+struct ScoreLaunch {
+    const uint16_t *q_idx;   // fp16 [T, H_I, 128]
+    const float *w;          // [T, H_I]
+    int H_I;
+    int hadamard_q;
+    float *scores;           // [rows, ld]
+    int64_t ld;
+    int fill_masked;         // write -inf for visible-range complements up to ld
+    RowMap rows;
+};
+cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const DevBatch &b,
+                         uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k,
+                        int32_t *idx, uint32_t *status, cudaStream_t stream);
+
+struct AttnLaunch {
+    int H, k;
+    float sm_scale;
+    const int32_t *idx;      // [T, k]
+    float *out;              // [T, H, 512]
+    float *lse;              // [T, H] or null
+    int tiles_per_cta;       // 128-row tiles handled by one CTA
+    int n_split;             // CTAs per (token, head group)
+    float *part_o;           // [T, n_split, groups*64, 512] when n_split > 1
+    float *part_ml;          // [T, n_split, groups*64, 2]
+};
+cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map,
+                               const CUtensorMap &q_rope_map, const CUtensorMap &kv_map,
+                               const DevBatch &b, uint32_t *status, cudaStream_t stream);
+cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream);
+
+// Shared-memory bytes of the attention kernel (for the host's occupancy set-up).
+size_t sparse_attn_smem_bytes();
+size_t score_smem_bytes(int n_pad, int hadamard_q);
+
+}  // namespace dsa

@@ -1,0 +1,394 @@
+// score.cu -- lightning-indexer score on the 5th-generation tensor cores.
+//
+// ik_llama_opt commit log, "Add GLM-5.2/DeepSeek-V3.2 DSA lightning indexer":
+//   scores = relu(indexer_k . indexer_q), scaled per-head weights, summed over
+//   heads, plus the causal mask.  The keys come from the persistent fp16
+//   single-head cache of "decode-correct via persistent indexer-K cache"
+//   (rotated queries when the cache holds rotated keys).
+//
+// One CTA owns a group of up to G query tokens of one sequence and a chunk of
+// consecutive 128-key tiles.  Per tile the tensor core computes
+//     D[key, (token, head)] = k_tile[128 x 128] . Q[(token, head) x 128]^T
+// (M = 128 keys, N = G * HP with HP = H_I rounded up to 16, K = 128) into a
+// double-buffered TMEM accumulator, so the epilogue of tile i overlaps the
+// MMA of tile i+1 and the TMA loads of tiles i+2.. .  In the epilogue each
+// thread owns one key row (its TMEM lane) and reduces sum_h w * max(0, D) for
+// each of its tokens in registers -- no cross-thread reduction.
+//
+// Warp roles: warp 0 issues TMA loads (4-stage ring of 32 KB key tiles),
+// warp 1 allocates TMEM and issues MMAs, warps 2..5 stage the queries and run
+// the epilogue.  All waits are bounded (1 s) and end in DSA_DEV_TIMEOUT.
+#include <algorithm>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileKeys = 128;
+constexpr int kTileBytes = kTileKeys * D_I * 2;  // 32 KB: two 64-column SW128 boxes
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+struct ScoreParams {
+    const uint16_t *q_idx;
+    const float *w;
+    float *scores;
+    int64_t ld;
+    DevBatch b;
+    uint32_t *status;
+    RowMap rows;
+    int H_I, HP, G, NP;       // heads, padded heads, tokens per group, padded N = G*HP
+    int hadamard_q;
+    int fill_masked;
+    int tiles_per_cta;
+    int groups_per_seq;
+    uint32_t tmem_cols;
+};
+
+struct Smem {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t q_ready;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+    int32_t pos[256];
+    int64_t out_row[256];
+    float w[256];
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Smem &sm,
+                                         uint32_t *status) {
+    if (*(volatile int32_t *)&sm.abort_flag) return false;
+    if (mbar_wait(bar, parity)) return true;
+    *(volatile int32_t *)&sm.abort_flag = 1;
+    flag(status, DSA_DEV_TIMEOUT);
+    return false;
+}
+
+// Rotate (optionally) one 128-element query row held 4 per lane, split into
+// fp16 hi (+ lo) parts and store them at row n of the SW128 K-major operand.
+__device__ __forceinline__ void stage_q_row(const uint16_t *src, bool valid, int hadamard,
+                                            uint8_t *q_hi, uint8_t *q_lo, int NP, int n, int lane) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+        const uint2 x = __ldg(reinterpret_cast<const uint2 *>(src) + lane);
+        v[0] = __half2float(__ushort_as_half((unsigned short)(x.x & 0xFFFF)));
+        v[1] = __half2float(__ushort_as_half((unsigned short)(x.x >> 16)));
+        v[2] = __half2float(__ushort_as_half((unsigned short)(x.y & 0xFFFF)));
+        v[3] = __half2float(__ushort_as_half((unsigned short)(x.y >> 16)));
+    }
+    uint16_t hi[4], lo[4];
+    if (hadamard) {
+        float a, c;
+        a = v[0]; c = v[1]; v[0] = a + c; v[1] = a - c;
+        a = v[2]; c = v[3]; v[2] = a + c; v[3] = a - c;
+        a = v[0]; c = v[2]; v[0] = a + c; v[2] = a - c;
+        a = v[1]; c = v[3]; v[1] = a + c; v[3] = a - c;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float other = __shfl_xor_sync(0xffffffffu, v[e], m);
+                v[e] = upper ? other - v[e] : v[e] + other;
+            }
+        }
+        const float scale = 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x = v[e] * scale;
+            const __half h = __float2half_rn(x);
+            hi[e] = __half_as_ushort(h);
+            lo[e] = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hi[e] = __half_as_ushort(__float2half_rn(v[e]));
+    }
+    // element 4*lane: K block lane/16, chunk (lane%16)/2, half-chunk lane%2
+    const int kb = lane >> 4;
+    const uint32_t off = (uint32_t)kb * (uint32_t)(NP * 128) +
+                         sw128_offset((uint32_t)n, (uint32_t)((lane & 15) >> 1)) + (lane & 1) * 8;
+    uint2 o;
+    o.x = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
+    o.y = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
+    *reinterpret_cast<uint2 *>(q_hi + off) = o;
+    if (hadamard) {
+        o.x = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
+        o.y = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
+        *reinterpret_cast<uint2 *>(q_lo + off) = o;
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    score_kernel(const ScoreParams p, const __grid_constant__ CUtensorMap k_map) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned operand region, then the control block.
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int q_bytes = p.NP * 256;                      // two 64-column K blocks
+    uint8_t *q_hi = base;
+    uint8_t *q_lo = base + q_bytes;                      // used with hadamard_q
+    uint8_t *stages = base + q_bytes * (p.hadamard_q ? 2 : 1);
+    Smem &sm = *reinterpret_cast<Smem *>(stages + kStages * kTileBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const DevBatch &b = p.b;
+
+    // ---- which tokens and keys this CTA covers (uniform across the CTA)
+    const int seq = blockIdx.y / p.groups_per_seq;
+    const int grp = blockIdx.y % p.groups_per_seq;
+    if (seq >= b.B) return;
+    const int q0 = __ldg(b.cu_q + seq), q1 = __ldg(b.cu_q + seq + 1);
+    const int n_seq = q1 - q0;
+    if (q0 < 0 || q1 > b.T || n_seq < 0 || n_seq > b.max_q) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && grp == 0) flag(p.status, DSA_DEV_BAD_POSITION);
+        return;
+    }
+    const int win_lo = p.rows.slab ? p.rows.j0 : 0;
+    const int win_hi = p.rows.slab ? min(p.rows.j0 + p.rows.J, n_seq) : n_seq;
+    const int j_lo = win_lo + grp * p.G;
+    const int j_hi = min(j_lo + p.G, win_hi);
+    if (j_lo >= j_hi) return;
+    const int g = j_hi - j_lo;
+    const int64_t kv0 = __ldg(b.kv_off + seq);
+
+    int max_p = -1;
+    for (int i = 0; i < g; ++i) {
+        const int pos = __ldg(b.q_pos + q0 + j_lo + i);
+        const bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0 && kv0 + pos < b.cache_rows;
+        if (ok) max_p = max(max_p, pos);
+    }
+    const int64_t chunk0 = (int64_t)blockIdx.x * p.tiles_per_cta * kTileKeys;
+    int n_mma = 0;
+    if (max_p >= chunk0)
+        n_mma = (int)min((int64_t)p.tiles_per_cta, (max_p - chunk0) / kTileKeys + 1);
+    int n_tiles = n_mma;
+    if (p.fill_masked) {
+        const int64_t left = p.ld - chunk0;
+        n_tiles = left <= 0 ? 0 : (int)min((int64_t)p.tiles_per_cta, (left + kTileKeys - 1) / kTileKeys);
+        n_tiles = max(n_tiles, n_mma);
+    }
+    if (n_tiles == 0) return;
+
+    // ---- set-up
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&sm.acc_full[s]), 1);
+            mbar_init(smem_u32(&sm.acc_empty[s]), kEpiWarps);
+        }
+        mbar_init(smem_u32(&sm.q_ready), kEpiWarps);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x < g && threadIdx.x < 256) {
+        const int i = threadIdx.x;
+        const int t = q0 + j_lo + i;
+        const int pos = __ldg(b.q_pos + t);
+        const bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0 && kv0 + pos < b.cache_rows;
+        if (!ok) flag(p.status, DSA_DEV_BAD_POSITION);
+        sm.pos[i] = ok ? pos : -1;
+        sm.out_row[i] = p.rows.slab ? (int64_t)seq * p.rows.J + (j_lo + i - p.rows.j0) : (int64_t)t;
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sm.tmem_base), p.tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&k_map);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            for (int i = 0; i < n_mma; ++i) {
+                const int s = i % kStages;
+                const uint32_t k = (uint32_t)(i / kStages);
+                if (!wait_bar(smem_u32(&sm.empty[s]), (k & 1) ^ 1, sm, p.status)) break;
+                const uint32_t full = smem_u32(&sm.full[s]);
+                mbar_arrive_expect_tx(full, kTileBytes);
+                const int32_t row = (int32_t)(kv0 + chunk0 + (int64_t)i * kTileKeys);
+                const uint32_t dst = smem_u32(stages + s * kTileBytes);
+                tma_load_2d(dst, &k_map, full, 0, row);
+                tma_load_2d(dst + kTileBytes / 2, &k_map, full, 64, row);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0 && wait_bar(smem_u32(&sm.q_ready), 0, sm, p.status)) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_f16(128, p.NP, false, false, false);
+            const uint32_t qh = smem_u32(q_hi), ql = smem_u32(q_lo);
+            const uint32_t qblk = (uint32_t)p.NP * 128u;
+            for (int i = 0; i < n_mma; ++i) {
+                const int s = i % kStages;
+                const uint32_t k = (uint32_t)(i / kStages);
+                const int buf = i & 1;
+                const uint32_t ka = (uint32_t)(i >> 1);
+                if (!wait_bar(smem_u32(&sm.acc_empty[buf]), (ka & 1) ^ 1, sm, p.status)) break;
+                if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * p.NP);
+                const uint32_t a0 = smem_u32(stages + s * kTileBytes);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t koff = (uint32_t)(kb * (kTileBytes / 2) + ks * 32);
+                        const uint64_t ad = sdesc_sw128(a0 + koff, 16, 1024);
+                        const uint32_t boff = (uint32_t)kb * qblk + (uint32_t)ks * 32;
+                        umma_f16(d, ad, sdesc_sw128(qh + boff, 16, 1024), idesc, (kb | ks) != 0);
+                        if (p.hadamard_q) umma_f16(d, ad, sdesc_sw128(ql + boff, 16, 1024), idesc, 1);
+                    }
+                }
+                umma_commit(smem_u32(&sm.empty[s]));
+                umma_commit(smem_u32(&sm.acc_full[buf]));
+            }
+        }
+    } else {
+        // ---------------- query staging + epilogue
+        const int ew = warp - 2;  // 0..kEpiWarps-1
+        // stage weights
+        for (int i = threadIdx.x - 64; i < p.G * p.HP; i += 32 * kEpiWarps) {
+            const int tok = i / p.HP, h = i % p.HP;
+            float wv = 0.f;
+            if (tok < g && h < p.H_I && sm.pos[tok] >= 0)
+                wv = __ldg(p.w + (int64_t)(q0 + j_lo + tok) * p.H_I + h);
+            sm.w[i] = wv;
+        }
+        // stage query rows n = tok*HP + h, one warp per row
+        for (int n = ew; n < p.NP; n += kEpiWarps) {
+            const int tok = n / p.HP, h = n % p.HP;
+            const bool valid = tok < g && h < p.H_I;
+            const uint16_t *src =
+                p.q_idx + ((int64_t)(q0 + j_lo + (valid ? tok : 0)) * p.H_I + (valid ? h : 0)) * D_I;
+            stage_q_row(src, valid, p.hadamard_q, q_hi, q_lo, p.NP, n, lane);
+        }
+        fence_proxy_async_smem();
+        named_barrier(1, 32 * kEpiWarps);     // weights and positions visible to all epilogue warps
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.q_ready));
+
+        const int quarter = warp & 3;         // TMEM lanes this warp may access
+        const int r = quarter * 32 + lane;    // key row within a tile
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const int hp16 = p.HP >> 4;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int64_t s = chunk0 + (int64_t)i * kTileKeys + r;
+            if (i < n_mma) {
+                const int buf = i & 1;
+                const uint32_t ka = (uint32_t)(i >> 1);
+                if (!wait_bar(smem_u32(&sm.acc_full[buf]), ka & 1, sm, p.status)) break;
+                tc_fence_after();
+                for (int tok = 0; tok < g; ++tok) {
+                    const uint32_t col = tmem + lane_addr + (uint32_t)(buf * p.NP + tok * p.HP);
+                    uint32_t v0[16], v1[16], v2[16], v3[16];
+                    tmem_ld16(col, v0);
+                    if (hp16 > 1) tmem_ld16(col + 16, v1);
+                    if (hp16 > 2) tmem_ld16(col + 32, v2);
+                    if (hp16 > 3) tmem_ld16(col + 48, v3);
+                    tmem_wait_ld();
+                    const float *wt = sm.w + tok * p.HP;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc = fmaf(wt[j], fmaxf(__uint_as_float(v0[j]), 0.f), acc);
+                    if (hp16 > 1) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            acc = fmaf(wt[16 + j], fmaxf(__uint_as_float(v1[j]), 0.f), acc);
+                    }
+                    if (hp16 > 2) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            acc = fmaf(wt[32 + j], fmaxf(__uint_as_float(v2[j]), 0.f), acc);
+                    }
+                    if (hp16 > 3) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            acc = fmaf(wt[48 + j], fmaxf(__uint_as_float(v3[j]), 0.f), acc);
+                    }
+                    const int pos = sm.pos[tok];
+                    float *dst = p.scores + sm.out_row[tok] * p.ld;
+                    if (s <= pos) dst[s] = acc;
+                    else if (p.fill_masked && s < p.ld) dst[s] = -INFINITY;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
+            } else {
+                for (int tok = 0; tok < g; ++tok)
+                    if (s < p.ld) p.scores[sm.out_row[tok] * p.ld + s] = -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+size_t score_smem_bytes(int n_pad, int hadamard_q) {
+    return 1024 + (size_t)n_pad * 256 * (hadamard_q ? 2 : 1) + (size_t)kStages * kTileBytes +
+           sizeof(Smem);
+}
+
+cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const DevBatch &b,
+                         uint32_t *status, cudaStream_t stream) {
+    ScoreParams p{};
+    p.q_idx = a.q_idx;
+    p.w = a.w;
+    p.scores = a.scores;
+    p.ld = a.ld;
+    p.b = b;
+    p.status = status;
+    p.rows = a.rows;
+    p.H_I = a.H_I;
+    p.HP = (a.H_I + 15) / 16 * 16;
+    const int n_max = a.hadamard_q ? 128 : 256;
+    const int window = a.rows.slab ? a.rows.J : b.max_q;
+    p.G = max(1, min(n_max / p.HP, window));
+    p.NP = p.G * p.HP;
+    p.hadamard_q = a.hadamard_q;
+    p.fill_masked = a.fill_masked;
+    p.groups_per_seq = (window + p.G - 1) / p.G;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * p.NP)) cols <<= 1;
+    p.tmem_cols = cols;
+
+    const int64_t span = a.fill_masked ? a.ld : (int64_t)b.max_kv;
+    const int64_t tiles = (span + kTileKeys - 1) / kTileKeys;
+    const int64_t work = tiles * (int64_t)b.B * p.groups_per_seq;
+    int64_t tpc = (work + 4 * 152 - 1) / (4 * 152);
+    tpc = std::max<int64_t>(4, std::min<int64_t>(64, tpc));
+    p.tiles_per_cta = (int)tpc;
+    const int64_t chunks = (tiles + tpc - 1) / tpc;
+    const int64_t groups = (int64_t)b.B * p.groups_per_seq;
+    if (groups > 65535 || chunks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+
+    const size_t smem = score_smem_bytes(p.NP, p.hadamard_q);
+    cudaError_t e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)chunks, (unsigned)groups);
+    score_kernel<<<grid, kThreads, smem, stream>>>(p, k_map);
+    return cudaGetLastError();
+}
+
+}  // namespace dsa

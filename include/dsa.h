@@ -1,0 +1,236 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek Sparse Attention hot path.
+ *
+ * The path: an fp16 single-head indexer-key cache, the lightning-indexer
+ * score I(t,s) = sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s]) under the causal mask
+ * s <= pos(t), a top-k selection of positions, and softmax attention of every
+ * query head over only the selected rows of the 576-wide MLA latent cache
+ * (512 latent + 64 rope tail), returning the 512-d latent output.
+ *
+ * Sources (page title, section):
+ *  [IDX]  ik_llama_opt commit log (src/llama-context.h page), commit "Add
+ *         GLM-5.2/DeepSeek-V3.2 DSA lightning indexer": the score formula,
+ *         the causal mask, ggml_top_k(min(top_k, n_tokens)).
+ *  [KC]   same page, commit "GLM-5.2 DSA indexer: decode-correct via
+ *         persistent indexer-K cache": the [128, kv_size] fp16 single-head
+ *         key cache written at the token's slot before scoring; the
+ *         Walsh-Hadamard rotation of q and k applied before the fp16 store.
+ *  [MLA]  ds4 PR #523 "hy3: Metal decode path + shared gate/up fusion",
+ *         milestone M3: 576-wide cached rows (kv_a latent + rotated rope
+ *         tail) and glm_mla_attention_one (scores over nope + rope parts,
+ *         one softmax across the candidate rows, values from the latent).
+ *  [ABS]  ik_llama_opt commit log, "MLA tensor parallelism under -sm graph":
+ *         wk_b / wv_b absorbed weights, so attention runs on the latent and
+ *         the value up-projection is applied by the caller.
+ *  [OPS]  vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on gfx1030",
+ *         "Prohibitions honored": out-arguments into caller buffers, no
+ *         blocking device-to-host copy, capture-safe calls.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named in the signatures are DEVICE pointers unless stated;
+ *    the caller owns every buffer.  The library never allocates, frees or
+ *    synchronises; all work is enqueued on `stream` (NULL = legacy default
+ *    stream) and returns before it runs.  No call reads device memory on the
+ *    host.  A call may be captured into a CUDA graph if the caller keeps
+ *    the arguments alive.
+ *  - Storage types: dsa_f16 is an IEEE binary16 bit pattern, dsa_bf16 a
+ *    bfloat16 bit pattern.  All tensors are dense, row-major, contiguous.
+ *  - Fixed dims: indexer head dim 128, latent 512, rope tail 64, row 576.
+ *    Supported: 1 <= H_I <= 64 indexer heads, 1 <= H <= 64 query heads,
+ *    1 <= k <= 65536.  Others return DSA_ERR_UNSUPPORTED.
+ *  - Device pointers passed to the TMA engine (k_cache, kv_cache, q_lat,
+ *    q_rope) must be 16-byte aligned, else DSA_ERR_MISALIGNED.
+ *  - Host validation runs before anything is enqueued; a failing call
+ *    enqueues nothing.  A failed launch returns DSA_ERR_CUDA.
+ *  - Device-detected problems (a position outside the stated bounds, an
+ *    index out of range, a bounded wait that gave up) never trap: the kernel
+ *    skips the offending work, ORs a DSA_DEV_* bit into the status word at
+ *    the start of the workspace and carries on.  dsa_read_device_status
+ *    reads and clears it.
+ *  - Inputs must be finite; NaN or Inf inputs give unspecified results.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t dsa_f16;
+typedef uint16_t dsa_bf16;
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size, bad enum */
+    DSA_ERR_UNSUPPORTED = 2,        /* a dimension outside the supported set */
+    DSA_ERR_MISALIGNED = 3,         /* a TMA-read pointer not 16-byte aligned */
+    DSA_ERR_WORKSPACE_TOO_SMALL = 4,
+    DSA_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+    DSA_ERR_DEVICE = 6              /* dsa_read_device_status found DSA_DEV_* bits */
+} dsa_status_t;
+
+/* Bits of the device status word. */
+enum {
+    DSA_DEV_BAD_POSITION = 1u << 0, /* q_pos / kv_off / cu_q outside the stated bounds */
+    DSA_DEV_BAD_INDEX    = 1u << 1, /* an idx entry not in {-1} U [0, q_pos[t]] */
+    DSA_DEV_TIMEOUT      = 1u << 2  /* a bounded wait on an mbarrier gave up */
+};
+
+/* dtype of new indexer keys */
+enum { DSA_KEY_F32 = 0, DSA_KEY_F16 = 1 };
+
+/* operations for dsa_workspace_size */
+enum {
+    DSA_OP_K_APPEND = 0,
+    DSA_OP_INDEXER_SCORE = 1,
+    DSA_OP_TOPK = 2,
+    DSA_OP_SPARSE_ATTN = 3,
+    DSA_OP_DECODE = 4
+};
+
+/*
+ * Variable-length batch.  B sequences, T query tokens in total; the tokens
+ * of sequence b are t = cu_q[b] .. cu_q[b+1]-1.  Token t sits at absolute
+ * position q_pos[t] within its sequence and sees the positions 0..q_pos[t]
+ * (the inclusive causal mask of [IDX]).  Sequence b owns rows
+ * kv_off[b] + s of both pooled caches (indexer keys and latent rows).
+ * The host fields are upper bounds used to size grids and must hold:
+ *   cu_q[b+1] - cu_q[b] <= max_q_per_seq,  q_pos[t] + 1 <= max_kv,
+ *   kv_off[b] + q_pos[t] < cache_rows.
+ * Positions are device data on purpose: a captured graph replays with new
+ * positions without being rebuilt.
+ */
+typedef struct {
+    int32_t batch;            /* B >= 1 (host) */
+    int32_t total_q;          /* T >= 1 (host) */
+    int32_t max_q_per_seq;    /* host upper bound, >= 1 */
+    int32_t max_kv;           /* host upper bound of visible positions, >= 1 */
+    int64_t cache_rows;       /* host: rows of each pooled cache */
+    const int32_t *cu_q;      /* device [B+1], cu_q[0] = 0, cu_q[B] = T */
+    const int32_t *q_pos;     /* device [T] */
+    const int64_t *kv_off;    /* device [B] */
+} dsa_batch_t;
+
+/*
+ * Indexer-key append ([KC]).  For every token t, writes
+ *   k_cache[kv_off[b] + q_pos[t], :] = fp16_rne(hadamard ? H k_new[t] / sqrt(128) : k_new[t])
+ * where H is the 128x128 Sylvester (natural order) Hadamard matrix.  The
+ * rotation is exact before the single rounding to fp16.
+ *   k_new    [T,128] float32 (k_dtype DSA_KEY_F32) or fp16 (DSA_KEY_F16)
+ *   k_cache  [cache_rows,128] fp16, updated in place (only the T rows)
+ *   ws       at least dsa_workspace_size(DSA_OP_K_APPEND) bytes (status word)
+ */
+dsa_status_t dsa_indexer_k_append(const void *k_new, int k_dtype, const dsa_batch_t *batch,
+                                  dsa_f16 *k_cache, int hadamard,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Lightning-indexer score, unfused ([IDX]; rotation per [KC]).
+ *   scores[t, s] = sum_h w[t,h] * max(0, q'[t,h] . k_cache[kv_off[b]+s])   for s <= q_pos[t]
+ *   scores[t, s] = -INFINITY                                               for q_pos[t] < s < ld_scores
+ * with q' = H q_idx[t,h] / sqrt(128) when hadamard_q (the keys in the cache
+ * are then expected rotated too), else q' = q_idx.  Products are formed
+ * from fp16 operands and accumulated in float32; with hadamard_q the rotated
+ * query is carried as two fp16 parts (hi + lo) so it keeps ~22 bits.
+ *   q_idx   [T,H_I,128] fp16      w [T,H_I] float32
+ *   k_cache [cache_rows,128] fp16 scores [T, ld_scores] float32, ld_scores >= max_kv
+ * Materialises the whole score matrix: meant for tests and small batches.
+ */
+dsa_status_t dsa_indexer_score(const dsa_f16 *q_idx, const float *w, const dsa_f16 *k_cache,
+                               const dsa_batch_t *batch, int H_I, int hadamard_q,
+                               float *scores, int64_t ld_scores,
+                               void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Top-k selection ([IDX]: ggml_top_k(min(top_k, n))).  For every token t the
+ * positions s in 0..q_pos[t] are ranked by (scores[t,s] descending,
+ * s ascending); -0.0 ranks equal to +0.0.  The first min(k, q_pos[t]+1) are
+ * written to idx[t, :] in ascending order of s, the remainder is -1.  The
+ * selected set is exact: bit-for-bit the same as a full sort of the given
+ * float32 values.
+ *   scores [T, ld_scores] float32 (only the visible prefix of each row is read)
+ *   idx    [T, k] int32 (sequence-local positions)
+ */
+dsa_status_t dsa_topk(const float *scores, int64_t ld_scores, const dsa_batch_t *batch, int k,
+                      int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Sparse MLA attention in the absorbed form ([MLA], [ABS]).  For token t and
+ * head h, over the selected rows c_j = kv_cache[kv_off[b] + idx[t,j]]:
+ *   z_j      = sm_scale * (q_lat[t,h] . c_j[0:512] + q_rope[t,h] . c_j[512:576])
+ *   out[t,h] = sum_j softmax(z)_j * c_j[0:512]
+ *   lse[t,h] = log(sum_j exp(z_j))                (natural log)
+ * Entries idx = -1 are skipped; a token with no valid entry gets out = 0 and
+ * lse = -INFINITY.  Entries outside [0, q_pos[t]] are skipped and flagged.
+ *   q_lat [T,H,512] bf16, q_rope [T,H,64] bf16, kv_cache [cache_rows,576] bf16
+ *   idx [T,k] int32, out [T,H,512] float32, lse [T,H] float32 or NULL
+ * bf16 operands, float32 accumulation and softmax; the probabilities enter the
+ * value product as bf16.
+ */
+dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope,
+                                 const dsa_bf16 *kv_cache, const dsa_batch_t *batch,
+                                 const int32_t *idx, int k, int H, float sm_scale,
+                                 float *out, float *lse, void *ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/*
+ * The fused step ([IDX], [KC], [MLA]): append the new indexer keys, score
+ * every query against its visible keys, select the top-k positions and
+ * attend over them -- in that stream order, so each token's own key is in
+ * the cache before scoring.  Decode (one token per sequence) and prefill
+ * chunks (many tokens of a sequence) use the same call.  Scores are kept in
+ * the workspace in slabs of query rows and never returned.
+ *   k_new [T,128] (k_dtype), q_idx [T,H_I,128] fp16, w [T,H_I] float32,
+ *   q_lat [T,H,512] bf16, q_rope [T,H,64] bf16,
+ *   k_cache [cache_rows,128] fp16 (updated), kv_cache [cache_rows,576] bf16
+ *   (already holding every row the queries can see, including their own),
+ *   out [T,H,512] float32, lse [T,H] float32 or NULL, idx_out [T,k] int32 or NULL.
+ * hadamard rotates both the appended keys and the queries.
+ */
+dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                        const dsa_bf16 *q_lat, const dsa_bf16 *q_rope,
+                        dsa_f16 *k_cache, const dsa_bf16 *kv_cache,
+                        const dsa_batch_t *batch, int H_I, int H, int k, float sm_scale,
+                        int hadamard, float *out, float *lse, int32_t *idx_out,
+                        void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Workspace bytes an operation needs for this batch (host only; batch
+ * pointers are not read).  Every workspace starts with the 256-byte status
+ * block; call dsa_workspace_init once on a new workspace.
+ */
+dsa_status_t dsa_workspace_size(int op, const dsa_batch_t *batch, int H_I, int H, int k,
+                                size_t *bytes);
+
+/* Zeroes the status block (enqueued on stream). */
+dsa_status_t dsa_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, copies the status word to *flags and clears it.
+ * Returns DSA_ERR_DEVICE when any DSA_DEV_* bit was set, else DSA_OK.
+ * This is the only call that synchronises; it is for tests and debugging.
+ */
+dsa_status_t dsa_read_device_status(void *ws, cudaStream_t stream, uint32_t *flags);
+
+/* Static description of a status code. */
+const char *dsa_status_string(dsa_status_t status);
+
+/*
+ * Profiling hook (not thread-safe).  When set, dsa_decode records
+ * events[0..n) on its stream at stage boundaries: before the append, the
+ * first score launch, the first top-k launch, the attention and the combine,
+ * and after the last launch (6 events).  n = 0 or events = NULL disables it.
+ */
+dsa_status_t dsa_set_trace_events(cudaEvent_t *events, int n);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H */

@@ -1,0 +1,118 @@
+"""The C-ABI library builds, loads and exports every symbol include/dsa.h
+declares; host-side validation answers before anything touches a device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import dsa_sparse_attention_score_gb300 as dsa
+from dsa_sparse_attention_score_gb300 import build as dsa_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    dsa_build.build()
+    return dsa.lib()
+
+
+def declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_path():
+    names = declared()
+    for n in ("dsa_indexer_k_append", "dsa_indexer_score", "dsa_topk", "dsa_sparse_mla_attn", "dsa_decode"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(L):
+    for name in declared():
+        assert hasattr(L, name), name
+    assert set(declared()) == set(dsa.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_status_strings(L):
+    assert dsa.dsa_version() == 10000
+    for code in range(0, 7):
+        assert dsa.dsa_status_string(code) not in ("", "unknown status")
+    assert dsa.dsa_status_string(99) == "unknown status"
+
+
+def _batch(**kw):
+    d = dict(batch=2, total_q=2, max_q_per_seq=1, max_kv=100, cache_rows=200,
+             cu_q=0x1000, q_pos=0x2000, kv_off=0x3000)
+    d.update(kw)
+    return dsa.dsa_batch_t(d["batch"], d["total_q"], d["max_q_per_seq"], d["max_kv"], d["cache_rows"],
+                           d["cu_q"], d["q_pos"], d["kv_off"])
+
+
+def test_workspace_sizes(L):
+    n = C.c_size_t()
+    b = _batch()
+    for op in range(5):
+        assert L.dsa_workspace_size(op, C.byref(b), 32, 64, 16, C.byref(n)) == dsa.DSA_OK
+        assert n.value >= 256 and n.value % 256 == 0
+    # decode: status + slab + idx + split partials
+    assert L.dsa_workspace_size(dsa.DSA_OP_DECODE, C.byref(b), 32, 64, 2048, C.byref(n)) == 0
+    assert n.value >= 256 + 2 * 100 * 4 + 2 * 2048 * 4
+    assert L.dsa_workspace_size(7, C.byref(b), 32, 64, 16, C.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_workspace_size(dsa.DSA_OP_TOPK, C.byref(b), 32, 64, 0, C.byref(n)) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_workspace_size(0, None, 32, 64, 16, C.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
+
+
+def test_argument_validation_runs_before_any_launch(L):
+    b = _batch()
+    ws, nws = C.c_void_p(0x10000), 1 << 20
+    fake = C.c_void_p(0x40000)          # never dereferenced: every call below fails validation
+    # null pointers
+    assert L.dsa_indexer_k_append(None, 0, C.byref(b), fake, 0, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_topk(fake, 100, None, 4, fake, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # bad dtype enum
+    assert L.dsa_indexer_k_append(fake, 7, C.byref(b), fake, 0, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # unsupported dims
+    assert L.dsa_indexer_score(fake, fake, fake, C.byref(b), 65, 0, fake, 100, ws, nws, None) == \
+        dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_indexer_score(fake, fake, fake, C.byref(b), 0, 0, fake, 100, ws, nws, None) == \
+        dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_topk(fake, 100, C.byref(b), 0, fake, ws, nws, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_topk(fake, 100, C.byref(b), 70000, fake, ws, nws, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_sparse_mla_attn(fake, fake, fake, C.byref(b), fake, 16, 65, 0.1, fake, None, ws, nws,
+                                 None) == dsa.DSA_ERR_UNSUPPORTED
+    # score row stride shorter than the visible span
+    assert L.dsa_topk(fake, 99, C.byref(b), 4, fake, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # misaligned TMA operands
+    odd = C.c_void_p(0x40008)
+    assert L.dsa_sparse_mla_attn(odd, fake, fake, C.byref(b), fake, 16, 8, 0.1, fake, None, ws, nws,
+                                 None) == dsa.DSA_ERR_MISALIGNED
+    assert L.dsa_indexer_k_append(fake, 0, C.byref(b), odd, 0, ws, nws, None) == dsa.DSA_ERR_MISALIGNED
+    # workspace
+    assert L.dsa_topk(fake, 100, C.byref(b), 4, fake, ws, 16, None) == dsa.DSA_ERR_WORKSPACE_TOO_SMALL
+    assert L.dsa_topk(fake, 100, C.byref(b), 4, fake, C.c_void_p(0x10010), nws, None) == dsa.DSA_ERR_MISALIGNED
+    n = C.c_size_t()
+    L.dsa_workspace_size(dsa.DSA_OP_DECODE, C.byref(b), 32, 64, 2048, C.byref(n))
+    assert L.dsa_decode(fake, 0, fake, fake, fake, fake, fake, fake, C.byref(b), 32, 64, 2048, 0.1, 0,
+                        fake, None, None, ws, n.value - 256, None) == dsa.DSA_ERR_WORKSPACE_TOO_SMALL
+    # inconsistent batch bounds
+    for kw in (dict(batch=0), dict(total_q=3, max_q_per_seq=1), dict(max_kv=0), dict(cache_rows=1 << 31),
+               dict(q_pos=0)):
+        bb = _batch(**kw)
+        assert L.dsa_topk(fake, 100, C.byref(bb), 4, fake, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_set_trace_events(None, -1) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_set_trace_events(None, 0) == dsa.DSA_OK
+    assert L.dsa_workspace_init(None, 256, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_workspace_init(ws, 100, None) == dsa.DSA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_product_path_never_touches_the_oracle():
+    """The library package imports nothing from oracle/ and ships no CPU path."""
+    pkg = os.path.dirname(dsa.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(root, f)).read()
+                assert "oracle" not in text.lower(), f
