@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Throughput of the DSA hot path (indexer-key append, lightning-indexer
+score, top-k, sparse MLA attention) on GB300.
+
+One step = one fused dsa_decode call over one batch of synthetic inputs
+already resident in HBM.  Default workload: batched decode, 8 sequences of
+8192 cached positions, 32 indexer heads x 128, 64 query heads, top-2048,
+576-wide bf16 latent rows.  The step is captured once into a CUDA graph and
+replayed; L2 is flushed (a 512 MB write) before every timed step and each
+step is timed with CUDA events on its stream.  The library's trace events
+split every timed step into its kernels, which gives the per-kernel
+durations behind the roofline object.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...    # the CPU oracle on the same workload
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas, no data-path collective); the reported time is the
+maximum over ranks and the value counts the tokens of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode tok/s & prefill tok/s on 1 GB300; % of HBM / tensor roofline"
+UNIT = "tok/s"
+WORKLOADS = {"tiny_decode": 1, "batched_decode": 2, "ragged_decode": 3, "prefill_chunk": 4, "long_prefill": 5}
+STAGES = ["k_append", "indexer_score", "topk", "sparse_attn", "attn_combine"]
+KERNEL_OF_STAGE = {"k_append": "k_append_kernel", "indexer_score": "score_kernel", "topk": "topk_kernel",
+                   "sparse_attn": "sparse_attn_kernel", "attn_combine": "attn_combine_kernel"}
+SOURCE_OF_KERNEL = {"k_append_kernel": "k_append.cu", "score_kernel": "score.cu", "topk_kernel": "topk.cu",
+                    "sparse_attn_kernel": "sparse_attn.cu", "attn_combine_kernel": "sparse_attn.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["dsa", "reference"], default="dsa")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched_decode")
+    ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="eager launches instead of a CUDA graph")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def algorithmic(wl):
+    """Bytes each step must move and flops it must do (per kernel), from the
+    workload shape: the indexer reads every visible key once per sequence
+    (256 B a row) and does 2*128 flops per (visible key, query, head); the
+    attention gathers the selected 1152-B latent rows once per query token
+    and does 2*(576+512) flops per (selected row, head)."""
+    key_rows = 0
+    for b in range(wl.B):
+        toks = range(wl.cu_q[b], wl.cu_q[b + 1])
+        key_rows += max(wl.q_pos[t] for t in toks) + 1 if len(toks) else 0
+    pairs = sum(p + 1 for p in wl.q_pos)
+    sel = sum(min(wl.top_k, p + 1) for p in wl.q_pos)
+    score_bytes = key_rows * 256
+    attn_bytes = sel * 1152
+    return dict(score_bytes=score_bytes, score_flops=pairs * wl.H_I * 256,
+                attn_bytes=attn_bytes, attn_flops=sel * wl.H * 2 * (576 + 512),
+                step_bytes=score_bytes + attn_bytes)
+
+
+def source_hash(kernel):
+    path = os.path.join(ROOT, "dsa_sparse_attention_score_gb300", "csrc", SOURCE_OF_KERNEL[kernel])
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel, {}).get(workload)
+    if not rec or rec.get("src_sha256_16") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.tmp = tempfile.NamedTemporaryFile(prefix="dsa_clocks_", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(gpu_index)], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.tmp.close()
+        rows = []
+        for line in open(self.tmp.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[2]), max=float(parts[3]), power=parts[4],
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], swp=parts[9]))
+            except ValueError:
+                continue
+        os.unlink(self.tmp.name)
+        return rows
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def gpu_index_for(device):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if device < len(ids) and ids[device].isdigit():
+            return int(ids[device])
+    return device
+
+
+# ---------------------------------------------------------------------------- oracle (CPU) legs
+
+def run_oracle_sample(wl, inp, seconds):
+    """Times the oracle's whole step on the full batch, repeated within the budget."""
+    import oracle
+    cores = oracle.set_threads(0)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(inp, wl)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 50:
+            break
+    return dict(value=wl.T * reps / el, unit=UNIT, cores=cores, kind="oracle",
+                sample=f"{reps} full steps of the {wl.name} workload ({wl.T} query tokens each), "
+                       f"{el:.1f} s of CPU time on {cores} OpenMP threads")
+
+
+def reference_arm(args):
+    """The CPU oracle as the reference implementation: each step decodes one
+    query token of the workload (its own sequence, all its keys)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import dsa_synth as S
+    import oracle
+    wl = S.config(WORKLOADS[args.workload])
+    inp = S.make_inputs(wl)
+    cores = oracle.set_threads(0)
+    subs = []
+    for t in range(wl.T if wl.T <= 64 else 64):
+        b = int(np.searchsorted(wl.cu_q, t, side="right") - 1)
+        off, p = wl.kv_off[b], wl.q_pos[t]
+        one = S.Workload(wl.name, wl.seed, [p + 1], [p], [0, 1], wl.H_I, wl.H, wl.top_k, wl.hadamard, wl.sm_scale)
+        sl = slice(off, off + p + 1)
+        subs.append((one, S.Inputs(k_cache=inp.k_cache[sl], k_new=inp.k_new[t:t + 1], q_idx=inp.q_idx[t:t + 1],
+                                   w=inp.w[t:t + 1], q_lat=inp.q_lat[t:t + 1], q_rope=inp.q_rope[t:t + 1],
+                                   kv_cache=inp.kv_cache[sl])))
+    for i in range(args.warmup):
+        one, si = subs[i % len(subs)]
+        oracle.decode(si, one)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one, si = subs[i % len(subs)]
+        oracle.decode(si, one)
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H_I": wl.H_I, "H": wl.H, "top_k": wl.top_k,
+                       "step": "one query token of the workload (its sequence's full key range)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} steps, one query token each, cycling over the "
+                                       f"{len(subs)} first tokens of {wl.name}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    from dsa_sparse_attention_score_gb300 import build as lib_build
+    if rank == 0 or world == 1:
+        lib_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    import dsa_sparse_attention_score_gb300 as dsa
+    import dsa_synth as S
+
+    wl = S.config(WORKLOADS[args.workload])
+    inp = S.make_inputs(wl)
+
+    def up(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    k_new, q_idx, w, q_lat, q_rope = up(inp.k_new), up(inp.q_idx), up(inp.w), up(inp.q_lat), up(inp.q_rope)
+    k_cache, kv_cache = up(inp.k_cache), up(inp.kv_cache)
+    batch = dsa.Batch.from_host(wl.cu_q, wl.q_pos, wl.kv_off, wl.cache_rows, max_q_per_seq=wl.max_q_per_seq,
+                                max_kv=wl.max_kv)
+    ws = dsa.workspace(dsa.DSA_OP_DECODE, batch, wl.H_I, wl.H, wl.top_k)
+    out = torch.empty((wl.T, wl.H, 512), device="cuda")
+    lse = torch.empty((wl.T, wl.H), device="cuda")
+    idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device="cuda")
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device="cuda")
+    launches = dsa.dsa_decode_launches(batch, wl.H_I, wl.H, wl.top_k)
+
+    trace = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    def step():
+        dsa.dsa_decode(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch, wl.top_k, wl.sm_scale,
+                       wl.hadamard, out, lse, idx, ws)
+
+    dsa.dsa_set_trace_events(trace)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        run()
+    torch.cuda.synchronize()
+    if dsa.dsa_read_device_status(ws) != 0:
+        raise RuntimeError("device status flags set during warm-up")
+
+    # ---- timed region
+    clocks = Clocks(gpu_index_for(dev))
+    time.sleep(0.2)                                  # let the sampler start
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    stage_ms = {s: [] for s in STAGES}
+    step_ms = []
+    n_split_stage = launches == 5                    # a combine kernel follows the attention
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        run()
+        trace[5].synchronize()
+        t = [trace[0].elapsed_time(trace[j]) for j in range(1, 6)]
+        step_ms.append(t[4])
+        stage_ms["k_append"].append(t[0])
+        stage_ms["indexer_score"].append(t[1] - t[0])
+        stage_ms["topk"].append(t[2] - t[1])
+        stage_ms["sparse_attn"].append(t[3] - t[2])
+        stage_ms["attn_combine"].append(t[4] - t[3])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_rows = clocks.stop()
+    dsa.dsa_set_trace_events(None)
+
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        tt = torch.tensor([total_s], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(tt.item())
+    ms_per_step = 1e3 * total_s / args.steps
+    value = world * wl.T * args.steps / total_s
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda a: (torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+                     if a.dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
+    h_in = [pin(inp.k_new), pin(inp.q_idx), pin(inp.w), pin(inp.q_lat), pin(inp.q_rope)]
+    d_in = [k_new, q_idx, w, q_lat, q_rope]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    e2e_ms = []
+    for i in range(n_e2e + 3):
+        flush.fill_(i & 0xFF)
+        e0.record()
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_s = sum(e2e_ms) / 1e3
+    if world > 1:
+        tt = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = world * wl.T * n_e2e / e2e_s
+    if dsa.dsa_read_device_status(ws) != 0:
+        raise RuntimeError("device status flags set during the timed steps")
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel
+    pk = peaks()
+    alg = algorithmic(wl)
+    mean = {s: statistics.fmean(v) for s, v in stage_ms.items()}
+    if not n_split_stage:
+        mean["attn_combine"] = 0.0
+    dom = max(mean, key=mean.get)
+    decode = wl.max_q_per_seq == 1
+    if dom == "indexer_score" and not decode:
+        achieved = alg["score_flops"] / (mean[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "dtype": "fp16", "algorithmic_flops_per_launch": alg["score_flops"]}
+    elif dom in ("indexer_score", "sparse_attn"):
+        nbytes = alg["score_bytes"] if dom == "indexer_score" else alg["attn_bytes"]
+        achieved = nbytes / (mean[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "algorithmic_bytes_per_launch": nbytes}
+    else:
+        roof = {"bound": "latency", "achieved": None, "peak": None, "unit": None}
+    if roof.get("achieved") is not None:
+        roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = KERNEL_OF_STAGE[dom]
+    roof["ms_per_launch"] = mean[dom]
+    roof["peak_source"] = f"{pk['source']} (MEASURED_PEAKS.json)" if pk["source"] == "measured" else "fallback"
+    roof["traffic"] = ncu_traffic(KERNEL_OF_STAGE[dom], wl.name)
+
+    step_gbs = alg["step_bytes"] / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16+bf16 (f32 accumulate)", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "L": wl.max_kv, "H_I": wl.H_I, "H": wl.H,
+                   "top_k": wl.top_k, "hadamard": wl.hadamard,
+                   "l2": f"flushed before every timed step ({args.flush_mb} MB write)",
+                   "launch": "CUDA graph replay" if graph is not None else "eager",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": Clocks.summary(clock_rows),
+        "gpu_launches": launches * args.steps,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": n_e2e, "path": "pinned H2D of the step inputs, dsa_decode through the Python "
+                                        "binding, D2H of the output; caches stay resident"},
+        "roofline": roof,
+        "step_roofline": {"bound": "hbm", "algorithmic_bytes": alg["step_bytes"], "achieved": step_gbs,
+                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": step_gbs / pk["hbm_gbs"]},
+        "stages_ms": {s: round(m, 5) for s, m in mean.items()},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_oracle_sample(wl, inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -62,6 +62,7 @@ SIGNATURES = {
     "dsa_decode": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _P, _P, _P, _P, _SZ, _P]),
     "dsa_workspace_size": (_I, [_I, _BP, _I, _I, _I, C.POINTER(C.c_size_t)]),
     "dsa_workspace_init": (_I, [_P, _SZ, _P]),
+    "dsa_decode_launches": (_I, [_BP, _I, _I, _I, C.POINTER(C.c_int)]),
     "dsa_read_device_status": (_I, [_P, _P, C.POINTER(C.c_uint32)]),
     "dsa_status_string": (C.c_char_p, [_I]),
     "dsa_set_trace_events": (_I, [_P, _I]),
@@ -157,6 +158,13 @@ def dsa_workspace_size(op: int, batch: Batch, H_I: int, H: int, k: int) -> int:
     n = C.c_size_t(0)
     d = dsa_batch_t(batch.B, batch.T, batch.max_q_per_seq, batch.max_kv, batch.cache_rows, None, None, None)
     _check(lib().dsa_workspace_size(op, C.byref(d), H_I, H, k, C.byref(n)), "dsa_workspace_size")
+    return n.value
+
+
+def dsa_decode_launches(batch: Batch, H_I: int, H: int, k: int) -> int:
+    n = C.c_int(0)
+    d = dsa_batch_t(batch.B, batch.T, batch.max_q_per_seq, batch.max_kv, batch.cache_rows, None, None, None)
+    _check(lib().dsa_decode_launches(C.byref(d), H_I, H, k, C.byref(n)), "dsa_decode_launches")
     return n.value
 
 

@@ -142,8 +142,14 @@ dsa_status_t check_ws(void *ws, size_t ws_bytes, size_t need) {
     return DSA_OK;
 }
 
+// Inside a stream capture a plain event record only orders the graph; an
+// external record node makes every replay record the event.
 inline void trace(int i, cudaStream_t s) {
-    if (g_trace && i < g_trace_n && g_trace[i]) cudaEventRecord(g_trace[i], s);
+    if (!(g_trace && i < g_trace_n && g_trace[i])) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+    cudaEventRecordWithFlags(g_trace[i], s,
+                             cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
 }
 
 #define DSA_TRY_CUDA(x)                      \
@@ -182,6 +188,22 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
 
 }  // namespace
 
+namespace dsa {
+cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes) {
+    static std::mutex mu;
+    static bool done[4][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || slot < 0 || slot >= 4) return cudaErrorInvalidValue;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[slot][dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done[slot][dev] = true;
+    return e;
+}
+}  // namespace dsa
+
 extern "C" {
 
 const char *dsa_status_string(dsa_status_t s) {
@@ -215,6 +237,19 @@ dsa_status_t dsa_workspace_size(int op, const dsa_batch_t *batch, int H_I, int H
     if ((op == DSA_OP_TOPK || op == DSA_OP_SPARSE_ATTN || op == DSA_OP_DECODE) && (k < 1 || k > 65536))
         return DSA_ERR_UNSUPPORTED;
     *bytes = layout(op, batch, k).total;
+    return DSA_OK;
+}
+
+dsa_status_t dsa_decode_launches(const dsa_batch_t *batch, int H_I, int H, int k, int *launches) {
+    (void)H_I;
+    (void)H;
+    if (!launches || !batch || batch->batch < 1 || batch->total_q < 1 || batch->max_q_per_seq < 1 ||
+        batch->max_kv < 1)
+        return DSA_ERR_INVALID_ARGUMENT;
+    if (k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    const Layout L = layout(DSA_OP_DECODE, batch, k);
+    const int slabs = (batch->max_q_per_seq + L.J - 1) / L.J;
+    *launches = 1 + 2 * slabs + 1 + (L.n_split > 1 ? 1 : 0);
     return DSA_OK;
 }
 

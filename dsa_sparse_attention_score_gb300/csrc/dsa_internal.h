@@ -61,6 +61,9 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
                                const DevBatch &b, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream);
 
+// Sets a kernel's dynamic shared-memory limit once per device.
+cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes);
+
 // Shared-memory bytes of the attention kernel (for the host's occupancy set-up).
 size_t sparse_attn_smem_bytes();
 size_t score_smem_bytes(int n_pad, int hadamard_q);

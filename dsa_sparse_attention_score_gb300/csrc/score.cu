@@ -383,8 +383,8 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     if (groups > 65535 || chunks > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
     const size_t smem = score_smem_bytes(p.NP, p.hadamard_q);
-    cudaError_t e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(score_kernel), 0,
+                                     score_smem_bytes(256, 1) > 232448 ? 232448 : score_smem_bytes(256, 1));
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)chunks, (unsigned)groups);
     score_kernel<<<grid, kThreads, smem, stream>>>(p, k_map);

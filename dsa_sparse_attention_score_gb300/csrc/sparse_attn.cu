@@ -466,8 +466,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     p.n_split = a.n_split;
     p.n_tiles = (a.k + kRows - 1) / kRows;
     const size_t smem = sparse_attn_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(sparse_attn_kernel), 1, smem);
     if (e != cudaSuccess) return e;
     if (a.n_split > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)b.T, (unsigned)a.n_split);

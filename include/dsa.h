@@ -206,6 +206,12 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
 dsa_status_t dsa_workspace_size(int op, const dsa_batch_t *batch, int H_I, int H, int k,
                                 size_t *bytes);
 
+/*
+ * Number of kernels one dsa_decode call enqueues for this batch (host only;
+ * batch pointers are not read).  For launch accounting and tracing.
+ */
+dsa_status_t dsa_decode_launches(const dsa_batch_t *batch, int H_I, int H, int k, int *launches);
+
 /* Zeroes the status block (enqueued on stream). */
 dsa_status_t dsa_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
 
