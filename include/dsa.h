@@ -199,6 +199,39 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
                         void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * dsa_decode without a workspace, for callers that cannot allocate device
+ * memory (a plugin inside a framework that owns all device allocations, code
+ * running under stream capture where an allocation would break the capture,
+ * an embedder with a memory budget fixed up front).  The paper has no
+ * counterpart: this is an integration aid, not a step of the method.
+ *
+ * Arguments, results and errors are those of dsa_decode; the scratch that
+ * dsa_decode would take from `ws` comes from a static 64 MiB device array
+ * inside the library instead.  Every GPU that loads the library holds that
+ * array until the process exits.  This call allocates nothing and calls no
+ * allocating routine.
+ *  - Limit: a batch whose dsa_workspace_size(DSA_OP_DECODE, ...) exceeds
+ *    64 MiB (67108864 bytes) is refused with DSA_ERR_WORKSPACE_TOO_SMALL
+ *    before anything touches the device.  Decode batches fit (for example
+ *    8 sequences x 8192 positions, or 32 sequences of up to 65536 positions,
+ *    top-2048); long prefill chunks need dsa_decode with a caller workspace.
+ *  - Set-up: the first call on a device, with that device current, looks up
+ *    the array's device address and clears its status block on `stream`.
+ *    Make that first call before any stream capture.
+ *  - Sharing: every call uses the same array and leaves its contents behind;
+ *    calls whose work overlaps on the GPU (different streams without an
+ *    ordering between them) race on it and must not be issued.
+ *  - Device-side status bits of these calls accumulate in the array and are
+ *    not reported; offending work is still skipped, never trapped.
+ */
+dsa_status_t dsa_decode_noalloc(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                                const dsa_bf16 *q_lat, const dsa_bf16 *q_rope,
+                                dsa_f16 *k_cache, const dsa_bf16 *kv_cache,
+                                const dsa_batch_t *batch, int H_I, int H, int k, float sm_scale,
+                                int hadamard, float *out, float *lse, int32_t *idx_out,
+                                cudaStream_t stream);
+
+/*
  * Workspace bytes an operation needs for this batch (host only; batch
  * pointers are not read).  Every workspace starts with the 256-byte status
  * block; call dsa_workspace_init once on a new workspace.
