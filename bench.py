@@ -278,55 +278,106 @@ def main():
     launches = dsa.dsa_decode_launches(batch, wl.H_I, wl.H, wl.top_k)
 
     trace = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    flush_r = torch.ones((args.flush_mb << 20) // 4, dtype=torch.float32, device="cuda")
+
+    def flush_l2(i):
+        # write a buffer larger than L2, then read another one, so the step
+        # starts with a cold L2 that holds no dirty lines of the flush itself
+        flush.fill_(i & 0xFF)
+        flush_r.amax()
 
     def step():
         dsa.dsa_decode(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch, wl.top_k, wl.sm_scale,
                        wl.hadamard, out, lse, idx, ws)
 
-    dsa.dsa_set_trace_events(trace)
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    graph = None
+    graph = graph_traced = None
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step()
+        dsa.dsa_set_trace_events(trace)
+        graph_traced = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_traced):
+            step()
+        dsa.dsa_set_trace_events(None)
         torch.cuda.synchronize()
     run = graph.replay if graph is not None else step
+    # a third capture with the device timeline on: real start/end of each
+    # kernel inside an overlapped step (the timeline buffer is baked in)
+    tl_buf = torch.zeros(10, dtype=torch.int64, device="cuda")
+    graph_tl = None
+    if graph is not None:
+        dsa.dsa_set_timeline(tl_buf)
+        graph_tl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_tl):
+            step()
+        dsa.dsa_set_timeline(None)
+        torch.cuda.synchronize()
+
+    def run_traced():
+        if graph_traced is not None:
+            graph_traced.replay()
+        else:
+            dsa.dsa_set_trace_events(trace)
+            step()
+            dsa.dsa_set_trace_events(None)
 
     for i in range(args.warmup):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
         run()
+        run_traced()
     torch.cuda.synchronize()
     if dsa.dsa_read_device_status(ws) != 0:
         raise RuntimeError("device status flags set during warm-up")
 
-    # ---- timed region
+    # ---- timed region: K steps, each on a cold L2, timed on the device
     clocks = Clocks(gpu_index_for(dev))
     time.sleep(0.2)                                  # let the sampler start
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    stage_ms = {s: [] for s in STAGES}
-    step_ms = []
-    n_split_stage = launches == 5                    # a combine kernel follows the attention
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
+        ev[i][0].record()
         run()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    # the same step with stage events (they serialise the stages): per-kernel time
+    stage_ms = {s: [] for s in STAGES}
+    for i in range(min(args.steps, 200)):
+        flush_l2(i)
+        run_traced()
         trace[5].synchronize()
         t = [trace[0].elapsed_time(trace[j]) for j in range(1, 6)]
-        step_ms.append(t[4])
         stage_ms["k_append"].append(t[0])
         stage_ms["indexer_score"].append(t[1] - t[0])
         stage_ms["topk"].append(t[2] - t[1])
         stage_ms["sparse_attn"].append(t[3] - t[2])
         stage_ms["attn_combine"].append(t[4] - t[3])
+    # the step with the device timeline: per-kernel [start, end] inside a step
+    tl = {s: [] for s in STAGES}
+    if graph_tl is not None:
+        big = torch.iinfo(torch.int64).max
+        for i in range(min(args.steps, 200)):
+            tl_buf[0::2] = big
+            tl_buf[1::2] = 0
+            flush_l2(i)
+            graph_tl.replay()
+            torch.cuda.synchronize()
+            v = tl_buf.tolist()
+            t0 = min(x for x in v[0::2] if x != big)
+            for j, s_ in enumerate(STAGES):
+                if v[2 * j] != big:
+                    tl[s_].append(((v[2 * j] - t0) / 1e3, (v[2 * j + 1] - t0) / 1e3))
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clock_rows = clocks.stop()
-    dsa.dsa_set_trace_events(None)
 
     total_s = sum(step_ms) / 1e3
     if world > 1:
@@ -348,7 +399,7 @@ def main():
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     e2e_ms = []
     for i in range(n_e2e + 3):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
         e0.record()
         for d, h in zip(d_in, h_in):
             d.copy_(h, non_blocking=True)
@@ -376,8 +427,8 @@ def main():
     pk = peaks()
     alg = algorithmic(wl)
     mean = {s: statistics.fmean(v) for s, v in stage_ms.items()}
-    if not n_split_stage:
-        mean["attn_combine"] = 0.0
+    timeline = {s: [round(statistics.median(a for a, _ in v), 2), round(statistics.median(b for _, b in v), 2)]
+                for s, v in tl.items() if v}
     dom = max(mean, key=mean.get)
     decode = wl.max_q_per_seq == 1
     if dom == "indexer_score" and not decode:
@@ -405,7 +456,8 @@ def main():
         "vs_baseline": None, "dtype": "fp16+bf16 (f32 accumulate)", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "L": wl.max_kv, "H_I": wl.H_I, "H": wl.H,
                    "top_k": wl.top_k, "hadamard": wl.hadamard,
-                   "l2": f"flushed before every timed step ({args.flush_mb} MB write)",
+                   "l2": f"flushed before every timed step ({args.flush_mb} MB write, then {args.flush_mb} MB "
+                         "read of another buffer)",
                    "launch": "CUDA graph replay" if graph is not None else "eager",
                    "parallelism": f"replicas x{world}"},
         "clocks": Clocks.summary(clock_rows),
@@ -417,6 +469,11 @@ def main():
         "step_roofline": {"bound": "hbm", "algorithmic_bytes": alg["step_bytes"], "achieved": step_gbs,
                           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": step_gbs / pk["hbm_gbs"]},
         "stages_ms": {s: round(m, 5) for s, m in mean.items()},
+        "stages_note": "per-kernel times from a second graph with stage events, which serialise the "
+                       "kernels that the headline graph overlaps (programmatic dependent launch)",
+        "timeline_us": timeline,
+        "timeline_note": "median [first CTA start, last CTA end] of each kernel inside an overlapped step, "
+                         "from the library's device timeline (globaltimer), relative to the first start",
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_oracle_sample(wl, inp, args.cpu_seconds)

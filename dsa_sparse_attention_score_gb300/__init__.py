@@ -67,6 +67,7 @@ SIGNATURES = {
     "dsa_read_device_status": (_I, [_P, _P, C.POINTER(C.c_uint32)]),
     "dsa_status_string": (C.c_char_p, [_I]),
     "dsa_set_trace_events": (_I, [_P, _I]),
+    "dsa_set_timeline": (_I, [_P]),
     "dsa_version": (_I, []),
 }
 
@@ -296,6 +297,11 @@ def dsa_set_trace_events(events):
 
 
 _TRACE_KEEP = None
+
+
+def dsa_set_timeline(buf):
+    """buf: CUDA int64/uint64 tensor of 10 slots, or None to disable."""
+    _check(lib().dsa_set_timeline(_ptr(buf)), "dsa_set_timeline")
 
 
 def dsa_status_string(code: int) -> str:

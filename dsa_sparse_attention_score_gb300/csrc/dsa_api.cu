@@ -18,6 +18,7 @@ constexpr int kSMs = 152;
 
 cudaEvent_t *g_trace = nullptr;
 int g_trace_n = 0;
+unsigned long long *g_timeline = nullptr;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -43,6 +44,7 @@ DevBatch dev_batch(const dsa_batch_t *b) {
     d.cu_q = b->cu_q;
     d.q_pos = b->q_pos;
     d.kv_off = b->kv_off;
+    d.timeline = g_timeline;
     return d;
 }
 
@@ -160,7 +162,7 @@ inline void trace(int i, cudaStream_t s) {
 dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const dsa_bf16 *kv_cache,
                            const dsa_batch_t *batch, const int32_t *idx, int k, int H, float sm_scale,
                            float *out, float *lse, void *ws, const Layout &L, cudaStream_t stream,
-                           bool traced) {
+                           bool traced, bool pdl) {
     const DevBatch db = dev_batch(batch);
     CUtensorMap ql, qr, kv;
     const uint64_t qrows = (uint64_t)batch->total_q * H;
@@ -180,9 +182,9 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     a.part_o = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_o) : nullptr;
     a.part_ml = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_ml) : nullptr;
-    DSA_TRY_CUDA(launch_sparse_attn(a, ql, qr, kv, db, status_ptr(ws), stream));
+    DSA_TRY_CUDA(launch_sparse_attn(a, ql, qr, kv, db, status_ptr(ws), stream, pdl));
     if (traced) trace(4, stream);
-    DSA_TRY_CUDA(launch_attn_combine(a, db, stream));
+    DSA_TRY_CUDA(launch_attn_combine(a, db, stream, true));
     return DSA_OK;
 }
 
@@ -228,6 +230,11 @@ dsa_status_t dsa_set_trace_events(cudaEvent_t *events, int n) {
     return DSA_OK;
 }
 
+dsa_status_t dsa_set_timeline(void *dev_buf) {
+    g_timeline = static_cast<unsigned long long *>(dev_buf);
+    return DSA_OK;
+}
+
 dsa_status_t dsa_workspace_size(int op, const dsa_batch_t *batch, int H_I, int H, int k, size_t *bytes) {
     (void)H_I;
     (void)H;
@@ -249,7 +256,7 @@ dsa_status_t dsa_decode_launches(const dsa_batch_t *batch, int H_I, int H, int k
     if (k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
     const Layout L = layout(DSA_OP_DECODE, batch, k);
     const int slabs = (batch->max_q_per_seq + L.J - 1) / L.J;
-    *launches = 1 + 2 * slabs + 1 + (L.n_split > 1 ? 1 : 0);
+    *launches = (batch->max_q_per_seq == 1 ? 0 : 1) + 2 * slabs + 1 + (L.n_split > 1 ? 1 : 0);
     return DSA_OK;
 }
 
@@ -307,7 +314,7 @@ dsa_status_t dsa_indexer_score(const dsa_f16 *q_idx, const float *w, const dsa_f
     a.ld = ld_scores;
     a.fill_masked = 1;
     a.rows = RowMap{0, 0, batch->max_q_per_seq};
-    DSA_TRY_CUDA(launch_score(a, km, dev_batch(batch), status_ptr(ws), stream));
+    DSA_TRY_CUDA(launch_score(a, km, dev_batch(batch), status_ptr(ws), stream, false));
     return DSA_OK;
 }
 
@@ -321,7 +328,7 @@ dsa_status_t dsa_topk(const float *scores, int64_t ld_scores, const dsa_batch_t 
     if (!aligned(scores, 4) || !aligned(idx, 4)) return DSA_ERR_MISALIGNED;
     if ((s = check_ws(ws, ws_bytes, kStatusBytes)) != DSA_OK) return s;
     DSA_TRY_CUDA(launch_topk(scores, ld_scores, dev_batch(batch), RowMap{0, 0, 1}, k, idx,
-                             status_ptr(ws), stream));
+                             status_ptr(ws), stream, false));
     return DSA_OK;
 }
 
@@ -340,7 +347,7 @@ dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, 
     const Layout L = layout(DSA_OP_SPARSE_ATTN, batch, k);
     if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
     return run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream,
-                         false);
+                         false, false);
 }
 
 dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
@@ -371,8 +378,12 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
     if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_cache, D_I, (uint64_t)batch->cache_rows, 64, 128))
         return DSA_ERR_CUDA;
 
+    // Decode batches (one query token per sequence) append inside the score
+    // kernel; batches with several tokens per sequence append first.
+    const bool fuse_append = batch->max_q_per_seq == 1;
     trace(0, stream);
-    DSA_TRY_CUDA(launch_k_append(k_new, k_dtype, db, k_cache, hadamard != 0, st, stream));
+    if (!fuse_append)
+        DSA_TRY_CUDA(launch_k_append(k_new, k_dtype, db, k_cache, hadamard != 0, st, stream));
     for (int j0 = 0; j0 < batch->max_q_per_seq; j0 += L.J) {
         ScoreLaunch a{};
         a.q_idx = q_idx;
@@ -383,13 +394,19 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
         a.ld = L.ld;
         a.fill_masked = 0;
         a.rows = RowMap{1, j0, L.J};
+        a.depends = fuse_append ? 0 : (j0 == 0 ? 1 : 2);
+        a.fuse_append = fuse_append;
+        a.k_new = k_new;
+        a.k_dtype = k_dtype;
+        a.k_cache = k_cache;
+        a.hadamard_k = hadamard != 0;
         if (j0 == 0) trace(1, stream);
-        DSA_TRY_CUDA(launch_score(a, km, db, st, stream));
+        DSA_TRY_CUDA(launch_score(a, km, db, st, stream, !(fuse_append && j0 == 0)));
         if (j0 == 0) trace(2, stream);
-        DSA_TRY_CUDA(launch_topk(slab, L.ld, db, a.rows, k, idx, st, stream));
+        DSA_TRY_CUDA(launch_topk(slab, L.ld, db, a.rows, k, idx, st, stream, true));
     }
     trace(3, stream);
-    s = run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream, true);
+    s = run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream, true, true);
     if (L.n_split <= 1) trace(4, stream);
     trace(5, stream);
     return s;

@@ -29,6 +29,27 @@ __device__ __forceinline__ void flag(uint32_t *status, uint32_t bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its writes are visible (a no-op without the launch
+// attribute), and allow the next grid to start its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Index of the sequence owning token t, found by a whole warp: each lane
+// tests one cu_q entry per pass, so B <= 32 costs one round trip.  cu_q is
+// non-decreasing, so the lanes with cu_q[b] <= t form a prefix.
+__device__ __forceinline__ int seq_of_warp(const int32_t *cu_q, int B, int t, int lane) {
+    int seq = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int b = base + lane;
+        const bool le = b < B && __ldg(cu_q + b) <= t;
+        const uint32_t m = __ballot_sync(0xffffffffu, le);
+        if (m) seq = base + 31 - __clz((int)m);
+        if (m != 0xffffffffu) break;
+    }
+    return seq;
+}
+
 // Index of the sequence owning token t (binary search in cu_q[0..B]).
 __device__ __forceinline__ int seq_of(const int32_t *cu_q, int B, int t) {
     int lo = 0, hi = B;  // invariant cu_q[lo] <= t < cu_q[hi]
@@ -48,6 +69,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Every wait inside a CTA is bounded by this; a wait that runs out sets
 // DSA_DEV_TIMEOUT and makes the CTA wind down.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Tracing: earliest start / latest end of a kernel's CTAs (globaltimer ns).
+__device__ __forceinline__ void tl_start(unsigned long long *tl, int slot) {
+    if (tl && threadIdx.x == 0) atomicMin(tl + 2 * slot, (unsigned long long)global_ns());
+}
+__device__ __forceinline__ void tl_end(unsigned long long *tl, int slot) {
+    if (tl && threadIdx.x == 0) atomicMax(tl + 2 * slot + 1, (unsigned long long)global_ns());
+}
 
 // ---------------------------------------------------------------- smem
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -6,9 +6,30 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dsa.h"
 
 namespace dsa {
+
+// Launch with the programmatic-stream-serialization attribute when `pdl` is
+// set: the kernel may start while its predecessor in the stream finishes and
+// must call griddepcontrol.wait before reading the predecessor's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DevBatch {
     int B, T;
@@ -17,7 +38,11 @@ struct DevBatch {
     const int32_t *cu_q;
     const int32_t *q_pos;
     const int64_t *kv_off;
+    unsigned long long *timeline;   // optional [2 * kTimelineSlots] start/end ns (tracing)
 };
+
+// Tracing slots of the kernels (earliest CTA start, latest CTA end).
+enum { kTlAppend = 0, kTlScore = 1, kTlTopk = 2, kTlAttn = 3, kTlCombine = 4, kTimelineSlots = 5 };
 
 // Rows of a score/top-k slab: either one row per token (direct) or the rows
 // (b, j - j0) of the local-token window [j0, j0 + J) of every sequence.
@@ -28,6 +53,8 @@ struct RowMap {
 
 cudaError_t launch_k_append(const void *k_new, int k_dtype, const DevBatch &b, uint16_t *k_cache,
                             int hadamard, uint32_t *status, cudaStream_t stream);
+// In the launchers below `pdl` marks a launch that follows another kernel of
+// the same call (programmatic dependent launch).
 
 struct ScoreLaunch {
     const uint16_t *q_idx;   // fp16 [T, H_I, 128]
@@ -38,12 +65,23 @@ struct ScoreLaunch {
     int64_t ld;
     int fill_masked;         // write -inf for visible-range complements up to ld
     RowMap rows;
+    // What the preceding kernel of the same call wrote: 0 nothing this launch
+    // reads or overwrites, 1 the tokens' own keys (the append), 2 anything
+    // (a top-k still reading the score slab) -- then nothing starts before it ends.
+    int depends;
+    // Decode batches (one query token per sequence): the score kernel appends
+    // each token's key itself instead of a separate append launch.
+    int fuse_append;
+    const void *k_new;       // [T, 128] of k_dtype
+    int k_dtype;
+    uint16_t *k_cache;       // written at the token's row
+    int hadamard_k;
 };
 cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const DevBatch &b,
-                         uint32_t *status, cudaStream_t stream);
+                         uint32_t *status, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k,
-                        int32_t *idx, uint32_t *status, cudaStream_t stream);
+                        int32_t *idx, uint32_t *status, cudaStream_t stream, bool pdl);
 
 struct AttnLaunch {
     int H, k;
@@ -58,8 +96,8 @@ struct AttnLaunch {
 };
 cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map,
                                const CUtensorMap &q_rope_map, const CUtensorMap &kv_map,
-                               const DevBatch &b, uint32_t *status, cudaStream_t stream);
-cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream);
+                               const DevBatch &b, uint32_t *status, cudaStream_t stream, bool pdl);
+cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream, bool pdl);
 
 // Sets a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes);

@@ -18,16 +18,14 @@ namespace dsa {
 __global__ void __launch_bounds__(128) k_append_kernel(const void *__restrict__ k_new, int k_dtype,
                                                        DevBatch b, uint16_t *__restrict__ k_cache,
                                                        int hadamard, uint32_t *status) {
+    pdl_trigger();  // the score kernel may start its prologue now
+    tl_start(b.timeline, kTlAppend);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 4 + warp;
     if (t >= b.T) return;
-    const int s = seq_of(b.cu_q, b.B, t);
+    // Independent loads first: position, this lane's four key values, and the
+    // sequence lookup (one cu_q entry per lane); then the sequence's offset.
     const int32_t pos = __ldg(b.q_pos + t);
-    const int64_t row = __ldg(b.kv_off + s) + pos;
-    if (pos < 0 || pos >= b.max_kv || row < 0 || row >= b.cache_rows) {
-        if (lane == 0) flag(status, DSA_DEV_BAD_POSITION);
-        return;
-    }
     double v[4];
     if (k_dtype == DSA_KEY_F32) {
         const float4 x = __ldg(reinterpret_cast<const float4 *>(k_new) + (int64_t)t * 32 + lane);
@@ -38,6 +36,12 @@ __global__ void __launch_bounds__(128) k_append_kernel(const void *__restrict__ 
         v[1] = __half2float(__ushort_as_half((unsigned short)(x.x >> 16)));
         v[2] = __half2float(__ushort_as_half((unsigned short)(x.y & 0xFFFF)));
         v[3] = __half2float(__ushort_as_half((unsigned short)(x.y >> 16)));
+    }
+    const int s = seq_of_warp(b.cu_q, b.B, t, lane);
+    const int64_t row = __ldg(b.kv_off + s) + pos;
+    if (pos < 0 || pos >= b.max_kv || row < 0 || row >= b.cache_rows) {
+        if (lane == 0) flag(status, DSA_DEV_BAD_POSITION);
+        return;
     }
     if (hadamard) {
         // element index i = 4*lane + e: bits 0-1 are e, bits 2-6 are the lane.
@@ -66,6 +70,8 @@ __global__ void __launch_bounds__(128) k_append_kernel(const void *__restrict__ 
     out.x = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
     out.y = (uint32_t)h[2] | ((uint32_t)h[3] << 16);
     reinterpret_cast<uint2 *>(k_cache + row * D_I)[lane] = out;
+    __syncwarp();
+    if (lane == 0 && b.timeline) atomicMax(b.timeline + 2 * kTlAppend + 1, (unsigned long long)global_ns());
 }
 
 cudaError_t launch_k_append(const void *k_new, int k_dtype, const DevBatch &b, uint16_t *k_cache,

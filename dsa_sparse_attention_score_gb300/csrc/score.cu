@@ -44,12 +44,19 @@ struct ScoreParams {
     int H_I, HP, G, NP;       // heads, padded heads, tokens per group, padded N = G*HP
     int hadamard_q;
     int fill_masked;
+    int depends;
+    int fuse_append;
+    const void *k_new;
+    int k_dtype;
+    uint16_t *k_cache;
+    int hadamard_k;
     int tiles_per_cta;
     int groups_per_seq;
     uint32_t tmem_cols;
 };
 
 struct Smem {
+    uint4 new_key[16];        // the appended key row (fp16, row-major), fused-append mode
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t acc_full[2];
@@ -57,6 +64,8 @@ struct Smem {
     uint64_t q_ready;
     uint32_t tmem_base;
     int32_t abort_flag;
+    int32_t meta_q0, meta_q1, meta_max_p;
+    int64_t meta_kv0;
     int32_t pos[256];
     int64_t out_row[256];
     float w[256];
@@ -71,18 +80,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Smem &sm
     return false;
 }
 
-// Rotate (optionally) one 128-element query row held 4 per lane, split into
-// fp16 hi (+ lo) parts and store them at row n of the SW128 K-major operand.
-__device__ __forceinline__ void stage_q_row(const uint16_t *src, bool valid, int hadamard,
-                                            uint8_t *q_hi, uint8_t *q_lo, int NP, int n, int lane) {
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (valid) {
-        const uint2 x = __ldg(reinterpret_cast<const uint2 *>(src) + lane);
-        v[0] = __half2float(__ushort_as_half((unsigned short)(x.x & 0xFFFF)));
-        v[1] = __half2float(__ushort_as_half((unsigned short)(x.x >> 16)));
-        v[2] = __half2float(__ushort_as_half((unsigned short)(x.y & 0xFFFF)));
-        v[3] = __half2float(__ushort_as_half((unsigned short)(x.y >> 16)));
-    }
+// One 128-element query row is held 4 values per lane (lane l: 4l..4l+3).
+__device__ __forceinline__ uint2 load_q_row(const uint16_t *src, bool valid, int lane) {
+    return valid ? __ldg(reinterpret_cast<const uint2 *>(src) + lane) : make_uint2(0u, 0u);
+}
+
+// Rotate (optionally) a query row, split it into fp16 hi (+ lo) parts and
+// store them at row n of the SW128 K-major operand.
+__device__ __forceinline__ void store_q_row(uint2 x, int hadamard, uint8_t *q_hi, uint8_t *q_lo, int NP,
+                                            int n, int lane) {
+    float v[4];
+    v[0] = __half2float(__ushort_as_half((unsigned short)(x.x & 0xFFFF)));
+    v[1] = __half2float(__ushort_as_half((unsigned short)(x.x >> 16)));
+    v[2] = __half2float(__ushort_as_half((unsigned short)(x.y & 0xFFFF)));
+    v[3] = __half2float(__ushort_as_half((unsigned short)(x.y >> 16)));
     uint16_t hi[4], lo[4];
     if (hadamard) {
         float a, c;
@@ -102,14 +113,14 @@ __device__ __forceinline__ void stage_q_row(const uint16_t *src, bool valid, int
         const float scale = 0.08838834764831845f;  // 1/sqrt(128)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float x = v[e] * scale;
-            const __half h = __float2half_rn(x);
+            const float y = v[e] * scale;
+            const __half h = __float2half_rn(y);
             hi[e] = __half_as_ushort(h);
-            lo[e] = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+            lo[e] = __half_as_ushort(__float2half_rn(y - __half2float(h)));
         }
     } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hi[e] = __half_as_ushort(__float2half_rn(v[e]));
+        hi[0] = (uint16_t)(x.x & 0xFFFF); hi[1] = (uint16_t)(x.x >> 16);
+        hi[2] = (uint16_t)(x.y & 0xFFFF); hi[3] = (uint16_t)(x.y >> 16);
     }
     // element 4*lane: K block lane/16, chunk (lane%16)/2, half-chunk lane%2
     const int kb = lane >> 4;
@@ -124,6 +135,47 @@ __device__ __forceinline__ void stage_q_row(const uint16_t *src, bool valid, int
         o.y = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
         *reinterpret_cast<uint2 *>(q_lo + off) = o;
     }
+}
+
+// The token's new key in storage form: lane l returns fp16 elements 4l..4l+3
+// of fp16(hadamard ? H k / sqrt(128) : k).  The transform runs in float64,
+// where every partial sum of the butterflies is exact for fp16 inputs, so the
+// single rounding to fp16 happens on the exact value.
+__device__ __forceinline__ uint2 appended_key(const void *k_new, int k_dtype, int t, int hadamard, int lane) {
+    double v[4];
+    if (k_dtype == DSA_KEY_F32) {
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(k_new) + (int64_t)t * 32 + lane);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
+        const uint2 x = __ldg(reinterpret_cast<const uint2 *>(k_new) + (int64_t)t * 32 + lane);
+        v[0] = __half2float(__ushort_as_half((unsigned short)(x.x & 0xFFFF)));
+        v[1] = __half2float(__ushort_as_half((unsigned short)(x.x >> 16)));
+        v[2] = __half2float(__ushort_as_half((unsigned short)(x.y & 0xFFFF)));
+        v[3] = __half2float(__ushort_as_half((unsigned short)(x.y >> 16)));
+    }
+    if (hadamard) {
+        double a, c;
+        a = v[0]; c = v[1]; v[0] = a + c; v[1] = a - c;
+        a = v[2]; c = v[3]; v[2] = a + c; v[3] = a - c;
+        a = v[0]; c = v[2]; v[0] = a + c; v[2] = a - c;
+        a = v[1]; c = v[3]; v[1] = a + c; v[3] = a - c;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const double other = __shfl_xor_sync(0xffffffffu, v[e], m);
+                v[e] = upper ? other - v[e] : v[e] + other;
+            }
+        }
+        const double scale = 1.0 / sqrt(128.0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] *= scale;
+    }
+    uint2 o;
+    o.x = (uint32_t)__half_as_ushort(__double2half(v[0])) | ((uint32_t)__half_as_ushort(__double2half(v[1])) << 16);
+    o.y = (uint32_t)__half_as_ushort(__double2half(v[2])) | ((uint32_t)__half_as_ushort(__double2half(v[3])) << 16);
+    return o;
 }
 
 }  // namespace
@@ -142,12 +194,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DevBatch &b = p.b;
+    tl_start(b.timeline, kTlScore);
 
     // ---- which tokens and keys this CTA covers (uniform across the CTA)
     const int seq = blockIdx.y / p.groups_per_seq;
     const int grp = blockIdx.y % p.groups_per_seq;
     if (seq >= b.B) return;
-    const int q0 = __ldg(b.cu_q + seq), q1 = __ldg(b.cu_q + seq + 1);
+    if (threadIdx.x == 0) {                       // three independent loads
+        sm.meta_q0 = __ldg(b.cu_q + seq);
+        sm.meta_q1 = __ldg(b.cu_q + seq + 1);
+        sm.meta_kv0 = __ldg(b.kv_off + seq);
+    }
+    __syncthreads();
+    const int q0 = sm.meta_q0, q1 = sm.meta_q1;
+    const int64_t kv0 = sm.meta_kv0;
     const int n_seq = q1 - q0;
     if (q0 < 0 || q1 > b.T || n_seq < 0 || n_seq > b.max_q) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && grp == 0) flag(p.status, DSA_DEV_BAD_POSITION);
@@ -159,14 +219,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j_hi = min(j_lo + p.G, win_hi);
     if (j_lo >= j_hi) return;
     const int g = j_hi - j_lo;
-    const int64_t kv0 = __ldg(b.kv_off + seq);
-
-    int max_p = -1;
-    for (int i = 0; i < g; ++i) {
-        const int pos = __ldg(b.q_pos + q0 + j_lo + i);
+    if ((int)threadIdx.x < g) {                   // the group's positions, in parallel
+        const int i = threadIdx.x;
+        const int t = q0 + j_lo + i;
+        const int pos = __ldg(b.q_pos + t);
         const bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0 && kv0 + pos < b.cache_rows;
-        if (ok) max_p = max(max_p, pos);
+        if (!ok) flag(p.status, DSA_DEV_BAD_POSITION);
+        sm.pos[i] = ok ? pos : -1;
+        sm.out_row[i] = p.rows.slab ? (int64_t)seq * p.rows.J + (j_lo + i - p.rows.j0) : (int64_t)t;
     }
+    __syncthreads();
+    int max_p = -1;
+    for (int i = 0; i < g; ++i) max_p = max(max_p, sm.pos[i]);
     const int64_t chunk0 = (int64_t)blockIdx.x * p.tiles_per_cta * kTileKeys;
     int n_mma = 0;
     if (max_p >= chunk0)
@@ -178,6 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_tiles = max(n_tiles, n_mma);
     }
     if (n_tiles == 0) return;
+    // With a single query token in the sequence, only the tile holding its own
+    // (just appended) key depends on the preceding kernel; otherwise all do.
+    int first_dependent = n_mma;
+    if (p.depends == 2 || (p.depends == 1 && n_seq > 1)) first_dependent = 0;
+    else if (p.depends == 1 && n_mma > 0 && (max_p - chunk0) / kTileKeys < p.tiles_per_cta)
+        first_dependent = n_mma - 1;
+    // Fused append: this CTA holds the tile of the token's own position.
+    const int append_tile = (p.fuse_append && n_seq == 1 && n_mma > 0 &&
+                             (max_p - chunk0) / kTileKeys < p.tiles_per_cta) ? n_mma - 1 : -1;
 
     // ---- set-up
     if (threadIdx.x == 0) {
@@ -193,24 +266,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x < g && threadIdx.x < 256) {
-        const int i = threadIdx.x;
-        const int t = q0 + j_lo + i;
-        const int pos = __ldg(b.q_pos + t);
-        const bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0 && kv0 + pos < b.cache_rows;
-        if (!ok) flag(p.status, DSA_DEV_BAD_POSITION);
-        sm.pos[i] = ok ? pos : -1;
-        sm.out_row[i] = p.rows.slab ? (int64_t)seq * p.rows.J + (j_lo + i - p.rows.j0) : (int64_t)t;
-    }
     if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_base), p.tmem_cols);
         tmem_relinquish();
+        if (append_tile >= 0) {
+            const int t = q0 + j_lo;
+            const uint2 kv = appended_key(p.k_new, p.k_dtype, t, p.hadamard_k, lane);
+            reinterpret_cast<uint2 *>(p.k_cache + (kv0 + max_p) * D_I)[lane] = kv;   // persist
+            reinterpret_cast<uint2 *>(sm.new_key)[lane] = kv;                        // staging
+        }
     }
     if (warp == 0 && lane == 0) tma_prefetch_desc(&k_map);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------- TMA producer
@@ -218,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < n_mma; ++i) {
                 const int s = i % kStages;
                 const uint32_t k = (uint32_t)(i / kStages);
+                if (i == first_dependent) pdl_wait();
                 if (!wait_bar(smem_u32(&sm.empty[s]), (k & 1) ^ 1, sm, p.status)) break;
                 const uint32_t full = smem_u32(&sm.full[s]);
                 mbar_arrive_expect_tx(full, kTileBytes);
@@ -242,6 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(smem_u32(&sm.acc_empty[buf]), (ka & 1) ^ 1, sm, p.status)) break;
                 if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status)) break;
                 tc_fence_after();
+                if (i == append_tile) {
+                    // replace the stale cache row loaded by TMA with the new key
+                    const uint32_t r = (uint32_t)(max_p - (chunk0 + (int64_t)i * kTileKeys));
+                    uint8_t *tile = stages + s * kTileBytes;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTileBytes / 2) + sw128_offset(r, c & 7)) =
+                            sm.new_key[c];
+                    fence_proxy_async_smem();
+                }
                 const uint32_t d = tmem + (uint32_t)(buf * p.NP);
                 const uint32_t a0 = smem_u32(stages + s * kTileBytes);
 #pragma unroll
@@ -270,13 +352,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wv = __ldg(p.w + (int64_t)(q0 + j_lo + tok) * p.H_I + h);
             sm.w[i] = wv;
         }
-        // stage query rows n = tok*HP + h, one warp per row
-        for (int n = ew; n < p.NP; n += kEpiWarps) {
-            const int tok = n / p.HP, h = n % p.HP;
-            const bool valid = tok < g && h < p.H_I;
-            const uint16_t *src =
-                p.q_idx + ((int64_t)(q0 + j_lo + (valid ? tok : 0)) * p.H_I + (valid ? h : 0)) * D_I;
-            stage_q_row(src, valid, p.hadamard_q, q_hi, q_lo, p.NP, n, lane);
+        // stage query rows n = tok*HP + h; each warp keeps 8 row loads in flight
+        for (int n0 = ew; n0 < p.NP; n0 += 8 * kEpiWarps) {
+            uint2 x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int n = n0 + u * kEpiWarps;
+                const int tok = n / p.HP, h = n % p.HP;
+                const bool valid = n < p.NP && tok < g && h < p.H_I;
+                x[u] = load_q_row(p.q_idx + ((int64_t)(q0 + j_lo + (valid ? tok : 0)) * p.H_I + (valid ? h : 0)) * D_I,
+                                  valid, lane);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int n = n0 + u * kEpiWarps;
+                if (n < p.NP) store_q_row(x[u], p.hadamard_q, q_hi, q_lo, p.NP, n, lane);
+            }
         }
         fence_proxy_async_smem();
         named_barrier(1, 32 * kEpiWarps);     // weights and positions visible to all epilogue warps
@@ -338,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    tl_end(b.timeline, kTlScore);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, p.tmem_cols);
@@ -350,7 +442,7 @@ size_t score_smem_bytes(int n_pad, int hadamard_q) {
 }
 
 cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const DevBatch &b,
-                         uint32_t *status, cudaStream_t stream) {
+                         uint32_t *status, cudaStream_t stream, bool pdl) {
     ScoreParams p{};
     p.q_idx = a.q_idx;
     p.w = a.w;
@@ -367,6 +459,12 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     p.NP = p.G * p.HP;
     p.hadamard_q = a.hadamard_q;
     p.fill_masked = a.fill_masked;
+    p.depends = a.depends;
+    p.fuse_append = a.fuse_append;
+    p.k_new = a.k_new;
+    p.k_dtype = a.k_dtype;
+    p.k_cache = a.k_cache;
+    p.hadamard_k = a.hadamard_k;
     p.groups_per_seq = (window + p.G - 1) / p.G;
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * p.NP)) cols <<= 1;
@@ -387,8 +485,7 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
                                      score_smem_bytes(256, 1) > 232448 ? 232448 : score_smem_bytes(256, 1));
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)chunks, (unsigned)groups);
-    score_kernel<<<grid, kThreads, smem, stream>>>(p, k_map);
-    return cudaGetLastError();
+    return launch_k(score_kernel, grid, dim3(kThreads), smem, stream, pdl, p, k_map);
 }
 
 }  // namespace dsa

@@ -129,8 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = blockIdx.x;
     const int split = blockIdx.y;
     if (t >= b.T) return;
-    const int seq = seq_of(b.cu_q, b.B, t);
+    pdl_trigger();
+    tl_start(b.timeline, kTlAttn);
     const int pos = __ldg(b.q_pos + t);
+    const int seq = seq_of_warp(b.cu_q, b.B, t, lane);
     const int64_t kv0 = __ldg(b.kv_off + seq);
     const int tile_lo = split * p.tiles_per_cta;
     const int tile_hi = min(p.n_tiles, tile_lo + p.tiles_per_cta);
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem_u32(q_s + kb * kQBlockBytes), &q_lat_map, qf, kb * 64, qrow);
             tma_load_2d(smem_u32(q_s + 8 * kQBlockBytes), &q_rope_map, qf, 0, qrow);
         }
+        pdl_wait();                                  // the indices come from the preceding kernel
         for (int it = 0; it < n_my; ++it) {
             const int e0 = (tile_lo + it) * kRows + lane * 4;
             int32_t rr[4];
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sw = warp - 2;                           // 0..3
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         if (tx < kHeads) ctl.m[tx] = -INFINITY;
+        pdl_wait();
         named_barrier(1, 128);
         float lpart[kHeads];
 #pragma unroll
@@ -413,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    tl_end(b.timeline, kTlAttn);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -422,35 +427,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merge split partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const float *__restrict__ part_o,
                                                            const float *__restrict__ part_ml,
-                                                           int n_split, int H, float *out, float *lse) {
+                                                           int n_split, int H, float *out, float *lse,
+                                                           unsigned long long *timeline) {
+    __shared__ float wgt[128];
+    __shared__ float ml[2][128];
     const int t = blockIdx.x, h = blockIdx.y;
     const int64_t base = (int64_t)t * n_split;
+    tl_start(timeline, kTlCombine);
+    pdl_wait();
+    for (int s = threadIdx.x; s < n_split; s += 128) {      // all split statistics at once
+        ml[0][s] = __ldg(part_ml + ((base + s) * kHeads + h) * 2);
+        ml[1][s] = __ldg(part_ml + ((base + s) * kHeads + h) * 2 + 1);
+    }
+    __syncthreads();
     float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldg(part_ml + ((base + s) * kHeads + h) * 2));
+    for (int s = 0; s < n_split; ++s) M = fmaxf(M, ml[0][s]);
     float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < n_split; ++s) {
-        const float m = __ldg(part_ml + ((base + s) * kHeads + h) * 2);
-        const float l = __ldg(part_ml + ((base + s) * kHeads + h) * 2 + 1);
-        if (m == -INFINITY) continue;
-        const float wgt = exp2f(m - M);
-        L += wgt * l;
+        const float w = ml[0][s] == -INFINITY ? 0.f : exp2f(ml[0][s] - M);
+        L += w * ml[1][s];
+        if (threadIdx.x == 0) wgt[s] = w;
+    }
+    __syncthreads();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = 0; s < n_split; ++s) {
+        const float w = wgt[s];
         const float4 o = __ldg(reinterpret_cast<const float4 *>(part_o + ((base + s) * kHeads + h) * D_L) +
                                threadIdx.x);
-        acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
+        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
     reinterpret_cast<float4 *>(out + ((int64_t)t * H + h) * D_L)[threadIdx.x] = acc;
     if (lse && threadIdx.x == 0)
         lse[(int64_t)t * H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    __syncthreads();
+    tl_end(timeline, kTlCombine);
 }
 
 size_t sparse_attn_smem_bytes() { return 1024 + kQBytes + kCBytes + sizeof(Ctl); }
 
 cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map,
                                const CUtensorMap &q_rope_map, const CUtensorMap &kv_map,
-                               const DevBatch &b, uint32_t *status, cudaStream_t stream) {
+                               const DevBatch &b, uint32_t *status, cudaStream_t stream, bool pdl) {
     AttnParams p{};
     p.idx = a.idx;
     p.out = a.out;
@@ -470,15 +490,16 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     if (e != cudaSuccess) return e;
     if (a.n_split > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)b.T, (unsigned)a.n_split);
-    sparse_attn_kernel<<<grid, kThreads, smem, stream>>>(p, q_lat_map, q_rope_map, kv_map);
-    return cudaGetLastError();
+    return launch_k(sparse_attn_kernel, grid, dim3(kThreads), smem, stream, pdl, p, q_lat_map, q_rope_map,
+                    kv_map);
 }
 
-cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream) {
+cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream, bool pdl) {
     if (a.n_split <= 1) return cudaSuccess;
+    if (a.n_split > 128) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)b.T, (unsigned)a.H);
-    attn_combine_kernel<<<grid, 128, 0, stream>>>(a.part_o, a.part_ml, a.n_split, a.H, a.out, a.lse);
-    return cudaGetLastError();
+    return launch_k(attn_combine_kernel, grid, dim3(128), 0, stream, pdl, (const float *)a.part_o,
+                    (const float *)a.part_ml, a.n_split, a.H, a.out, a.lse, b.timeline);
 }
 
 }  // namespace dsa

@@ -266,6 +266,17 @@ const char *dsa_status_string(dsa_status_t status);
  */
 dsa_status_t dsa_set_trace_events(cudaEvent_t *events, int n);
 
+/*
+ * Tracing hook (not thread-safe).  When dev_buf is a device buffer of 10
+ * uint64 values, every kernel the library launches afterwards records the
+ * globaltimer (ns) of its earliest CTA start into dev_buf[2*i] (atomic min)
+ * and of its latest CTA end into dev_buf[2*i+1] (atomic max), i = 0 append,
+ * 1 score, 2 top-k, 3 attention, 4 combine.  The caller initialises the
+ * slots (start slots to UINT64_MAX, end slots to 0).  Unlike trace events
+ * this leaves the launch order and overlap untouched.  NULL disables it.
+ */
+dsa_status_t dsa_set_timeline(void *dev_buf);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int dsa_version(void);
 
