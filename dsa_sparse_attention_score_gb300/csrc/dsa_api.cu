@@ -15,6 +15,10 @@ constexpr int kVersion = 10000;  // 1.0.0
 constexpr size_t kAlign = 256;
 constexpr int64_t kSlabBytes = int64_t(1) << 30;  // score slab budget in the workspace
 constexpr int kSMs = 152;
+// Reduce the split-KV partials of a token inside a thread-block cluster
+// (distributed shared memory) instead of through the workspace and a combine
+// kernel.  Off: measured slower on GB300 with scalar remote stores.
+constexpr bool kClusterReduce = false;
 
 cudaEvent_t *g_trace = nullptr;
 int g_trace_n = 0;
@@ -179,6 +183,7 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
     a.lse = lse;
     a.n_split = L.n_split;
     a.tiles_per_cta = L.tiles_per_cta;
+    a.clustered = kClusterReduce && L.n_split > 1 && attn_cluster_ok(L.n_split);
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     a.part_o = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_o) : nullptr;
     a.part_ml = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_ml) : nullptr;
@@ -256,7 +261,8 @@ dsa_status_t dsa_decode_launches(const dsa_batch_t *batch, int H_I, int H, int k
     if (k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
     const Layout L = layout(DSA_OP_DECODE, batch, k);
     const int slabs = (batch->max_q_per_seq + L.J - 1) / L.J;
-    *launches = (batch->max_q_per_seq == 1 ? 0 : 1) + 2 * slabs + 1 + (L.n_split > 1 ? 1 : 0);
+    const bool combine = L.n_split > 1 && !(kClusterReduce && attn_cluster_ok(L.n_split));
+    *launches = (batch->max_q_per_seq == 1 ? 0 : 1) + 2 * slabs + 1 + (combine ? 1 : 0);
     return DSA_OK;
 }
 

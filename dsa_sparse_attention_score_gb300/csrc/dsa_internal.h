@@ -93,6 +93,7 @@ struct AttnLaunch {
     int n_split;             // CTAs per (token, head group)
     float *part_o;           // [T, n_split, groups*64, 512] when n_split > 1
     float *part_ml;          // [T, n_split, groups*64, 2]
+    int clustered;           // reduce the splits of a token inside a thread-block cluster
 };
 cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map,
                                const CUtensorMap &q_rope_map, const CUtensorMap &kv_map,
@@ -101,6 +102,9 @@ cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStre
 
 // Sets a kernel's dynamic shared-memory limit once per device.
 cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes);
+
+// Whether a token's n_split attention CTAs can run as one cluster here.
+bool attn_cluster_ok(int n_split);
 
 // Shared-memory bytes of the attention kernel (for the host's occupancy set-up).
 size_t sparse_attn_smem_bytes();

@@ -30,7 +30,7 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kTileKeys = 128;
 constexpr int kTileBytes = kTileKeys * D_I * 2;  // 32 KB: two 64-column SW128 boxes
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;   // two warps per TMEM lane quarter, splitting the tokens
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 struct ScoreParams {
@@ -57,6 +57,7 @@ struct ScoreParams {
 
 struct Smem {
     uint4 new_key[16];        // the appended key row (fp16, row-major), fused-append mode
+    float4 w4[64];            // head weights of the group's tokens (HP per token)
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t acc_full[2];
@@ -68,7 +69,6 @@ struct Smem {
     int64_t meta_kv0;
     int32_t pos[256];
     int64_t out_row[256];
-    float w[256];
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Smem &sm,
@@ -281,7 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    pdl_trigger();
 
     if (warp == 0) {
         // ---------------- TMA producer
@@ -350,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float wv = 0.f;
             if (tok < g && h < p.H_I && sm.pos[tok] >= 0)
                 wv = __ldg(p.w + (int64_t)(q0 + j_lo + tok) * p.H_I + h);
-            sm.w[i] = wv;
+            reinterpret_cast<float *>(sm.w4)[i] = wv;
         }
         // stage query rows n = tok*HP + h; each warp keeps 8 row loads in flight
         for (int n0 = ew; n0 < p.NP; n0 += 8 * kEpiWarps) {
@@ -375,9 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&sm.q_ready));
 
         const int quarter = warp & 3;         // TMEM lanes this warp may access
+        const int half = ew >> 2;             // which half of the group's tokens
         const int r = quarter * 32 + lane;    // key row within a tile
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int hp16 = p.HP >> 4;
+        const int tpw = (g + 1) >> 1;
+        const int tok_lo = half * tpw, tok_hi = min(g, tok_lo + tpw);
         for (int i = 0; i < n_tiles; ++i) {
             const int64_t s = chunk0 + (int64_t)i * kTileKeys + r;
             if (i < n_mma) {
@@ -385,43 +387,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ka = (uint32_t)(i >> 1);
                 if (!wait_bar(smem_u32(&sm.acc_full[buf]), ka & 1, sm, p.status)) break;
                 tc_fence_after();
-                for (int tok = 0; tok < g; ++tok) {
+                // two tokens' accumulators per TMEM round trip
+                for (int tok = tok_lo; tok < tok_hi; tok += 2) {
+                    const bool two = tok + 1 < tok_hi;
                     const uint32_t col = tmem + lane_addr + (uint32_t)(buf * p.NP + tok * p.HP);
-                    uint32_t v0[16], v1[16], v2[16], v3[16];
-                    tmem_ld16(col, v0);
-                    if (hp16 > 1) tmem_ld16(col + 16, v1);
-                    if (hp16 > 2) tmem_ld16(col + 32, v2);
-                    if (hp16 > 3) tmem_ld16(col + 48, v3);
+                    uint32_t v[8][16];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (c < hp16) tmem_ld16(col + 16 * c, v[c]);
+                    if (two) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (c < hp16) tmem_ld16(col + p.HP + 16 * c, v[4 + c]);
+                    }
                     tmem_wait_ld();
-                    const float *wt = sm.w + tok * p.HP;
-                    float acc = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc = fmaf(wt[j], fmaxf(__uint_as_float(v0[j]), 0.f), acc);
-                    if (hp16 > 1) {
+                    for (int u = 0; u < 2; ++u) {
+                        if (u == 1 && !two) break;
+                        const int tk = tok + u;
+                        const float4 *wt = sm.w4 + (tk * p.HP >> 2);   // broadcast 16-byte loads
+                        float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            acc = fmaf(wt[16 + j], fmaxf(__uint_as_float(v1[j]), 0.f), acc);
+                        for (int c = 0; c < 4; ++c) {
+                            if (c < hp16) {
+#pragma unroll
+                                for (int j = 0; j < 16; j += 4) {
+                                    const float4 w = wt[4 * c + (j >> 2)];
+                                    const float2 r01 = make_float2(fmaxf(__uint_as_float(v[4 * u + c][j]), 0.f),
+                                                                   fmaxf(__uint_as_float(v[4 * u + c][j + 1]), 0.f));
+                                    const float2 r23 = make_float2(fmaxf(__uint_as_float(v[4 * u + c][j + 2]), 0.f),
+                                                                   fmaxf(__uint_as_float(v[4 * u + c][j + 3]), 0.f));
+                                    acc2 = __ffma2_rn(make_float2(w.x, w.y), r01, acc2);
+                                    acc2 = __ffma2_rn(make_float2(w.z, w.w), r23, acc2);
+                                }
+                            }
+                        }
+                        const float acc = acc2.x + acc2.y;
+                        const int pos = sm.pos[tk];
+                        float *dst = p.scores + sm.out_row[tk] * p.ld;
+                        if (s <= pos) dst[s] = acc;
+                        else if (p.fill_masked && s < p.ld) dst[s] = -INFINITY;
                     }
-                    if (hp16 > 2) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            acc = fmaf(wt[32 + j], fmaxf(__uint_as_float(v2[j]), 0.f), acc);
-                    }
-                    if (hp16 > 3) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            acc = fmaf(wt[48 + j], fmaxf(__uint_as_float(v3[j]), 0.f), acc);
-                    }
-                    const int pos = sm.pos[tok];
-                    float *dst = p.scores + sm.out_row[tok] * p.ld;
-                    if (s <= pos) dst[s] = acc;
-                    else if (p.fill_masked && s < p.ld) dst[s] = -INFINITY;
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
             } else {
-                for (int tok = 0; tok < g; ++tok)
+                for (int tok = tok_lo; tok < tok_hi; ++tok)
                     if (s < p.ld) p.scores[sm.out_row[tok] * p.ld + s] = -INFINITY;
             }
         }
@@ -429,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    pdl_trigger();   // late: waiting dependents would share the SMs
     tl_end(b.timeline, kTlScore);
     if (warp == 1) {
         tc_fence_after();

@@ -54,6 +54,7 @@ struct AttnParams {
     int H, k;
     float scale_log2;        // sm_scale * log2(e)
     int tiles_per_cta, n_split, n_tiles;
+    int clustered;           // the n_split CTAs of a token form one cluster and reduce in DSMEM
 };
 
 struct Ctl {
@@ -69,6 +70,10 @@ struct Ctl {
     float m[kHeads];
     float alpha[kHeads];
     float l[kHeads];
+    float gm[kHeads];        // cluster-wide maximum per head
+    float gl[kHeads];        // cluster-wide softmax denominator per head
+    float sc[kHeads];        // this CTA's scale 2^(m - gm)
+    int32_t warp_alive[4];
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl &c, uint32_t *status) {
@@ -111,6 +116,33 @@ __device__ __forceinline__ void warp_reduce_64(const float (&x)[64], int lane, f
     r1 = a[1];
 }
 
+// One tile needs 288 gather4 requests (32 row quads x 9 column blocks).
+// Lane `gl` of the `kIssuers` issuing lanes sends requests gl, gl + kIssuers,
+// ... after the block it writes has been released by the previous tile.
+constexpr int kIssueWarps = 5;                 // producer + the four softmax warps
+constexpr int kIssuers = 32 * kIssueWarps;
+
+__device__ __forceinline__ bool issue_tile_gathers(int gl, int tile, const int32_t *idx_row, int k, int pos,
+                                                   int64_t kv0, uint32_t parity, uint8_t *c_s, Ctl &ctl,
+                                                   const CUtensorMap *kv_map, uint32_t *status) {
+    for (int q = gl; q < 32 * kBlocks; q += kIssuers) {
+        const int kb = q >> 5, quad = q & 31;
+        if (!wait_bar(smem_u32(&ctl.c_empty[kb]), parity, ctl, status)) return false;
+        int32_t rr[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = tile * kRows + quad * 4 + j;
+            const int32_t v = e < k ? __ldg(idx_row + e) : -1;
+            const bool ok = v >= 0 && v <= pos;
+            if (!ok && v != -1 && kb == 0) flag(status, DSA_DEV_BAD_INDEX);
+            rr[j] = (int32_t)(kv0 + (ok ? v : 0));
+        }
+        tma_gather4(smem_u32(c_s + kb * kCBlockBytes + quad * 512), kv_map, smem_u32(&ctl.c_full[kb]), kb * 64,
+                    rr[0], rr[1], rr[2], rr[3]);
+    }
+    return true;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -129,7 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = blockIdx.x;
     const int split = blockIdx.y;
     if (t >= b.T) return;
-    pdl_trigger();
     tl_start(b.timeline, kTlAttn);
     const int pos = __ldg(b.q_pos + t);
     const int seq = seq_of_warp(b.cu_q, b.B, t, lane);
@@ -195,27 +226,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pdl_wait();                                  // the indices come from the preceding kernel
         for (int it = 0; it < n_my; ++it) {
-            const int e0 = (tile_lo + it) * kRows + lane * 4;
-            int32_t rr[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int e = e0 + j;
-                const int32_t v = e < p.k ? __ldg(idx_row + e) : -1;
-                const bool ok = v >= 0 && v <= pos;
-                if (!ok && v != -1) flag(p.status, DSA_DEV_BAD_INDEX);
-                rr[j] = (int32_t)(kv0 + (ok ? v : 0));
-            }
             const uint32_t par = ((uint32_t)it & 1u) ^ 1u;
-            bool ok = true;
-            for (int kb = 0; kb < kBlocks; ++kb) {
-                if (!wait_bar(smem_u32(&ctl.c_empty[kb]), par, ctl, p.status)) { ok = false; break; }
-                const uint32_t cf = smem_u32(&ctl.c_full[kb]);
-                if (lane == 0) mbar_arrive_expect_tx(cf, kCBlockBytes);
-                __syncwarp();
-                tma_gather4(smem_u32(c_s + kb * kCBlockBytes + lane * 512), &kv_map, cf, kb * 64,
-                            rr[0], rr[1], rr[2], rr[3]);
+            if (lane == 0) {
+                bool ok = true;
+                for (int kb = 0; kb < kBlocks && ok; ++kb) {
+                    ok = wait_bar(smem_u32(&ctl.c_empty[kb]), par, ctl, p.status);
+                    if (ok) mbar_arrive_expect_tx(smem_u32(&ctl.c_full[kb]), kCBlockBytes);
+                }
+                if (!ok) break;
             }
-            if (!ok) break;
+            __syncwarp();
+            if (!issue_tile_gathers(lane, tile_lo + it, idx_row, p.k, pos, kv0, par, c_s, ctl, &kv_map, p.status))
+                break;
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
@@ -265,6 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         if (tx < kHeads) ctl.m[tx] = -INFINITY;
         pdl_wait();
+        const int gl = 32 + tx;                            // issuing lane id (producer warp owns 0..31)
+        bool alive = issue_tile_gathers(gl, tile_lo, idx_row, p.k, pos, kv0, 1u, c_s, ctl, &kv_map, p.status);
+        alive = __all_sync(0xffffffffu, alive);
         named_barrier(1, 128);
         float lpart[kHeads];
 #pragma unroll
@@ -272,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Every softmax thread runs the same sequence of named barriers whatever
         // happens; `alive` (warp-uniform) only gates tensor-memory and shared
         // memory work after a bounded wait gave up.
-        bool alive = true;
         for (int it = 0; it < n_my; ++it) {
             const uint32_t par = (uint32_t)it & 1u;
             const int e = (tile_lo + it) * kRows + r;
@@ -366,6 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl.p_full));
+            if (it + 1 < n_my && alive) {
+                // this warp's share of the next tile's gathers, as its blocks free up
+                alive = issue_tile_gathers(gl, tile_lo + it + 1, idx_row, p.k, pos, kv0, par, c_s,
+                                           ctl, &kv_map, p.status);
+            }
+            alive = __all_sync(0xffffffffu, alive);
         }
         // ---- final: O^T of the last tile, row sums, outputs
         const uint32_t last_par = (uint32_t)(n_my - 1) & 1u;
@@ -377,10 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctl.red[sw][2 * lane + 1] = l1;
         named_barrier(1, 128);
         if (tx < kHeads) ctl.l[tx] = ctl.red[0][tx] + ctl.red[1][tx] + ctl.red[2][tx] + ctl.red[3][tx];
+        if (lane == 0) ctl.warp_alive[sw] = alive ? 1 : 0;
         named_barrier(1, 128);
-        if (alive) {
+        if (alive && !p.clustered) {
+            // Stage this CTA's [head][dim] block in the dead gathered tile and
+            // write it with one bulk copy: unnormalised partials when the token
+            // is split, the normalised output otherwise.
             tc_fence_after();
             const int H = p.H;
+            const int rows = p.n_split > 1 ? kHeads : H;
+            float *stage = reinterpret_cast<float *>(c_s);
             for (int c = 0; c < 4; ++c) {
                 const int d = c * 128 + r;
 #pragma unroll
@@ -391,15 +427,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int h = half * 32 + j;
-                        const float o = __uint_as_float(u[j]);
-                        if (p.n_split > 1) {
-                            p.part_o[(((int64_t)t * p.n_split + split) * kHeads + h) * D_L + d] = o;
-                        } else if (h < H) {
+                        float o = __uint_as_float(u[j]);
+                        if (p.n_split == 1) {
                             const float l = ctl.l[h];
-                            p.out[((int64_t)t * H + h) * D_L + d] = l > 0.f ? o / l : 0.f;
+                            o = l > 0.f ? o / l : 0.f;
                         }
+                        if (h < rows) stage[h * D_L + d] = o;
                     }
                 }
+            }
+            fence_proxy_async_smem();
+        }
+        named_barrier(1, 128);                       // every warp, whatever its state
+        const bool all_alive = ctl.warp_alive[0] && ctl.warp_alive[1] && ctl.warp_alive[2] && ctl.warp_alive[3];
+        if (all_alive && !p.clustered) {
+            const int H = p.H;
+            const int rows = p.n_split > 1 ? kHeads : H;
+            if (tx == 0) {
+                float *dst = p.n_split > 1 ? p.part_o + ((int64_t)t * p.n_split + split) * kHeads * D_L
+                                           : p.out + (int64_t)t * H * D_L;
+                const uint32_t bytes = (uint32_t)(rows * D_L * 4);
+                for (uint32_t off = 0; off < bytes; off += 32768)
+                    bulk_s2g(reinterpret_cast<uint8_t *>(dst) + off, smem_u32(c_s) + off, min(32768u, bytes - off));
+                bulk_commit();
+                bulk_wait_all();
             }
             if (tx < kHeads) {
                 const int h = tx;
@@ -417,6 +468,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (p.clustered) {
+        // ---- split-KV reduction inside the cluster (the token's n_split CTAs):
+        // every CTA scales its unnormalised O^T by 2^(m - M) and sends each
+        // output slice to the CTA that owns it; owners sum the slices in a
+        // fixed order and write the normalised result.
+        const int CS = p.n_split;
+        const uint32_t my = cluster_rank();
+        const bool ok = ctl.warp_alive[0] && ctl.warp_alive[1] && ctl.warp_alive[2] && ctl.warp_alive[3];
+        const int tx = (int)threadIdx.x - 64;
+        if (!ok && tx >= 0 && tx < kHeads) {                // a CTA that gave up contributes nothing
+            ctl.m[tx] = -INFINITY;
+            ctl.l[tx] = 0.f;
+        }
+        cluster_sync_all();                                  // every m, l final; every PV done
+        const int dpo = D_L / CS;                            // output dims owned per CTA
+        const uint32_t slot_bytes = (uint32_t)(kHeads * dpo * 4);
+        const uint32_t recv = smem_u32(c_s);                 // the dead gathered tile holds the slots
+        if (warp >= 2) {
+            if (tx < kHeads) {
+                float M = -INFINITY;
+                for (int c = 0; c < CS; ++c) M = fmaxf(M, dsmem_ld_f32(dsmem_map(smem_u32(&ctl.m[tx]), c)));
+                float L = 0.f;
+                for (int c = 0; c < CS; ++c) {
+                    const float mc = dsmem_ld_f32(dsmem_map(smem_u32(&ctl.m[tx]), c));
+                    const float lc = dsmem_ld_f32(dsmem_map(smem_u32(&ctl.l[tx]), c));
+                    if (mc != -INFINITY) L += exp2f(mc - M) * lc;
+                }
+                ctl.gm[tx] = M;
+                ctl.gl[tx] = L;
+                ctl.sc[tx] = ctl.m[tx] == -INFINITY ? 0.f : exp2f(ctl.m[tx] - M);
+            }
+            named_barrier(1, 128);
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + (threadIdx.x & 31);
+            const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+            if (ok) tc_fence_after();
+            for (int c = 0; c < 4; ++c) {
+                const int d = c * 128 + r;
+                const uint32_t owner = (uint32_t)(d / dpo);
+                const uint32_t dst = dsmem_map(recv + my * slot_bytes, owner) + (uint32_t)((d % dpo) * 4);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t u[32];
+                    if (ok) {
+                        tmem_ld32(tmem + lane_addr + kColO + c * kHeads + half * 32, u);
+                        tmem_wait_ld();
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int h = half * 32 + j;
+                        const float v = ok ? __uint_as_float(u[j]) * ctl.sc[h] : 0.f;
+                        dsmem_st_f32(dst + (uint32_t)(h * dpo * 4), v);
+                    }
+                }
+            }
+        }
+        cluster_sync_all();                                  // every slice delivered
+        if (warp >= 2) {
+            const int H = p.H;
+            const uint8_t *slots = c_s;
+            for (int e = tx; e < kHeads * dpo; e += 128) {
+                const int h = e / dpo, dd = e % dpo;
+                float acc = 0.f;
+                for (int c = 0; c < CS; ++c)
+                    acc += *reinterpret_cast<const float *>(slots + c * slot_bytes + (h * dpo + dd) * 4);
+                if (h < H) {
+                    const float L = ctl.gl[h];
+                    p.out[((int64_t)t * H + h) * D_L + my * dpo + dd] = L > 0.f ? acc / L : 0.f;
+                }
+            }
+            if (my == 0 && p.lse && tx < H) {
+                const float L = ctl.gl[tx];
+                p.lse[(int64_t)t * H + tx] = L > 0.f ? (ctl.gm[tx] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+            }
+        }
+    }
+    // Dependents launch only now: CTAs of the next grid waiting on this one
+    // would share the SMs and slow it down.
+    pdl_trigger();
     tl_end(b.timeline, kTlAttn);
     if (warp == 1) {
         tc_fence_after();
@@ -450,12 +580,20 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float *__restri
     }
     __syncthreads();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = 0; s < n_split; ++s) {
-        const float w = wgt[s];
-        const float4 o = __ldg(reinterpret_cast<const float4 *>(part_o + ((base + s) * kHeads + h) * D_L) +
-                               threadIdx.x);
-        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+    for (int s0 = 0; s0 < n_split; s0 += 16) {              // 16 loads in flight
+        float4 o[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (s0 + u < n_split)
+                o[u] = __ldg(reinterpret_cast<const float4 *>(part_o + ((base + s0 + u) * kHeads + h) * D_L) +
+                             threadIdx.x);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            if (s0 + u < n_split) {
+                const float w = wgt[s0 + u];
+                acc.x += w * o[u].x; acc.y += w * o[u].y; acc.z += w * o[u].z; acc.w += w * o[u].w;
+            }
+        }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
@@ -489,13 +627,68 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(sparse_attn_kernel), 1, smem);
     if (e != cudaSuccess) return e;
     if (a.n_split > 65535) return cudaErrorInvalidConfiguration;
+    p.clustered = a.clustered;
     dim3 grid((unsigned)b.T, (unsigned)a.n_split);
-    return launch_k(sparse_attn_kernel, grid, dim3(kThreads), smem, stream, pdl, p, q_lat_map, q_rope_map,
-                    kv_map);
+    if (!a.clustered)
+        return launch_k(sparse_attn_kernel, grid, dim3(kThreads), smem, stream, pdl, p, q_lat_map, q_rope_map,
+                        kv_map);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)a.n_split;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, sparse_attn_kernel, p, q_lat_map, q_rope_map, kv_map);
+}
+
+// Whether the n_split CTAs of a token can run as one cluster on this device
+// (cluster sizes above 8 need the non-portable opt-in and a GPC with that
+// many free SMs).  Cached per device and size.
+bool attn_cluster_ok(int n_split) {
+    if (n_split < 2 || n_split > 16 || (n_split & (n_split - 1))) return false;
+    static int cache[64][17];                 // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    int &c = cache[dev][n_split];
+    if (c) return c == 1;
+    c = 2;
+    const size_t smem = sparse_attn_smem_bytes();
+    if (ensure_smem_attr(reinterpret_cast<const void *>(sparse_attn_kernel), 1, smem) != cudaSuccess) return false;
+    if (n_split > 8 && cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                           cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, (unsigned)n_split);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)n_split;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_attn_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (n > 0) c = 1;
+    return n > 0;
 }
 
 cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream, bool pdl) {
-    if (a.n_split <= 1) return cudaSuccess;
+    if (a.n_split <= 1 || a.clustered) return cudaSuccess;
     if (a.n_split > 128) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)b.T, (unsigned)a.H);
     return launch_k(attn_combine_kernel, grid, dim3(128), 0, stream, pdl, (const float *)a.part_o,

@@ -286,10 +286,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
                                                             DevBatch b, RowMap rows, int k,
                                                             int32_t *__restrict__ idx, uint32_t *status,
                                                             int cap) {
-    pdl_trigger();
     tl_start(b.timeline, kTlTopk);
     topk_row(scores, ld, b, rows, k, idx, status, cap);
     __syncthreads();
+    pdl_trigger();   // late: waiting dependents would share the SMs
     tl_end(b.timeline, kTlTopk);
 }
 
