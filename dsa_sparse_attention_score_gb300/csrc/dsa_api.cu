@@ -14,7 +14,6 @@ namespace {
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr size_t kAlign = 256;
 constexpr int64_t kSlabBytes = int64_t(1) << 30;  // score slab budget in the workspace
-constexpr int kSMs = 152;
 // Reduce the split-KV partials of a token inside a thread-block cluster
 // (distributed shared memory) instead of through the workspace and a combine
 // kernel.  Off: measured slower on GB300 with scalar remote stores.
@@ -198,11 +197,11 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
 namespace dsa {
 cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes) {
     static std::mutex mu;
-    static bool done[4][64] = {};
+    static bool done[kSmemAttrSlots][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || slot < 0 || slot >= 4) return cudaErrorInvalidValue;
+    if (dev < 0 || dev >= 64 || slot < 0 || slot >= kSmemAttrSlots) return cudaErrorInvalidValue;
     std::lock_guard<std::mutex> lock(mu);
     if (done[slot][dev]) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);

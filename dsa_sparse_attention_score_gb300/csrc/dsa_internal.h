@@ -31,6 +31,8 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+constexpr int kSMs = 152;   // streaming multiprocessors of the target GPU
+
 struct DevBatch {
     int B, T;
     int max_q, max_kv;
@@ -101,6 +103,9 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
 cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream, bool pdl);
 
 // Sets a kernel's dynamic shared-memory limit once per device.
+// Sets a kernel's dynamic shared-memory limit once per device; `slot`
+// (0..kSmemAttrSlots-1) names the kernel instance.
+constexpr int kSmemAttrSlots = 8;
 cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes);
 
 // Whether a token's n_split attention CTAs can run as one cluster here.
@@ -108,6 +113,6 @@ bool attn_cluster_ok(int n_split);
 
 // Shared-memory bytes of the attention kernel (for the host's occupancy set-up).
 size_t sparse_attn_smem_bytes();
-size_t score_smem_bytes(int n_pad, int hadamard_q);
+size_t score_smem_bytes(int n_pad, int hadamard_q, int n_stages);
 
 }  // namespace dsa

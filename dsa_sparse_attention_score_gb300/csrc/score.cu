@@ -27,11 +27,18 @@ namespace dsa {
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;        // depth of the key-tile ring (runtime: 2..4)
 constexpr int kTileKeys = 128;
 constexpr int kTileBytes = kTileKeys * D_I * 2;  // 32 KB: two 64-column SW128 boxes
-constexpr int kEpiWarps = 8;   // two warps per TMEM lane quarter, splitting the tokens
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Epilogue warps per CTA: 8 (two per TMEM lane quarter, splitting a group's
+// tokens, two tokens per TMEM round trip) for multi-token groups; 4 (one
+// token per round trip, fewer registers, several CTAs per SM) for decode.
+template <int kEpi> struct ScoreCfg {
+    static constexpr int kEpiWarps = kEpi;
+    static constexpr int kThreads = 64 + 32 * kEpi;
+    static constexpr int kTokPerWait = kEpi == 8 ? 2 : 1;
+    static constexpr int kHalves = kEpi / 4;
+};
 
 struct ScoreParams {
     const uint16_t *q_idx;
@@ -51,6 +58,7 @@ struct ScoreParams {
     uint16_t *k_cache;
     int hadamard_k;
     int tiles_per_cta;
+    int stages;
     int groups_per_seq;
     uint32_t tmem_cols;
 };
@@ -58,8 +66,8 @@ struct ScoreParams {
 struct Smem {
     uint4 new_key[16];        // the appended key row (fp16, row-major), fused-append mode
     float4 w4[64];            // head weights of the group's tokens (HP per token)
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t q_ready;
@@ -180,8 +188,12 @@ __device__ __forceinline__ uint2 appended_key(const void *k_new, int k_dtype, in
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kEpi>
+__global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi == 8 ? 1 : 2)
     score_kernel(const ScoreParams p, const __grid_constant__ CUtensorMap k_map) {
+    constexpr int kEpiWarps = ScoreCfg<kEpi>::kEpiWarps;
+    constexpr int kTokPerWait = ScoreCfg<kEpi>::kTokPerWait;
+    constexpr int kHalves = ScoreCfg<kEpi>::kHalves;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned operand region, then the control block.
     uint8_t *base = reinterpret_cast<uint8_t *>(
@@ -190,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *q_hi = base;
     uint8_t *q_lo = base + q_bytes;                      // used with hadamard_q
     uint8_t *stages = base + q_bytes * (p.hadamard_q ? 2 : 1);
-    Smem &sm = *reinterpret_cast<Smem *>(stages + kStages * kTileBytes);
+    const int n_stages = p.stages;
+    Smem &sm = *reinterpret_cast<Smem *>(stages + n_stages * kTileBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DevBatch &b = p.b;
@@ -254,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- set-up
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < n_stages; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
@@ -286,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- TMA producer
         if (lane == 0) {
             for (int i = 0; i < n_mma; ++i) {
-                const int s = i % kStages;
-                const uint32_t k = (uint32_t)(i / kStages);
+                const int s = i % n_stages;
+                const uint32_t k = (uint32_t)(i / n_stages);
                 if (i == first_dependent) pdl_wait();
                 if (!wait_bar(smem_u32(&sm.empty[s]), (k & 1) ^ 1, sm, p.status)) break;
                 const uint32_t full = smem_u32(&sm.full[s]);
@@ -306,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t qh = smem_u32(q_hi), ql = smem_u32(q_lo);
             const uint32_t qblk = (uint32_t)p.NP * 128u;
             for (int i = 0; i < n_mma; ++i) {
-                const int s = i % kStages;
-                const uint32_t k = (uint32_t)(i / kStages);
+                const int s = i % n_stages;
+                const uint32_t k = (uint32_t)(i / n_stages);
                 const int buf = i & 1;
                 const uint32_t ka = (uint32_t)(i >> 1);
                 if (!wait_bar(smem_u32(&sm.acc_empty[buf]), (ka & 1) ^ 1, sm, p.status)) break;
@@ -374,12 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&sm.q_ready));
 
         const int quarter = warp & 3;         // TMEM lanes this warp may access
-        const int half = ew >> 2;             // which half of the group's tokens
+        const int half = ew >> 2;             // which part of the group's tokens
         const int r = quarter * 32 + lane;    // key row within a tile
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int hp16 = p.HP >> 4;
-        const int tpw = (g + 1) >> 1;
-        const int tok_lo = half * tpw, tok_hi = min(g, tok_lo + tpw);
+        const int tpw = (g + kHalves - 1) / kHalves;
+        const int tok_lo = min(g, half * tpw), tok_hi = min(g, tok_lo + tpw);
         for (int i = 0; i < n_tiles; ++i) {
             const int64_t s = chunk0 + (int64_t)i * kTileKeys + r;
             if (i < n_mma) {
@@ -388,21 +401,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(smem_u32(&sm.acc_full[buf]), ka & 1, sm, p.status)) break;
                 tc_fence_after();
                 // two tokens' accumulators per TMEM round trip
-                for (int tok = tok_lo; tok < tok_hi; tok += 2) {
-                    const bool two = tok + 1 < tok_hi;
+                for (int tok = tok_lo; tok < tok_hi; tok += kTokPerWait) {
+                    const bool two = kTokPerWait == 2 && tok + 1 < tok_hi;
                     const uint32_t col = tmem + lane_addr + (uint32_t)(buf * p.NP + tok * p.HP);
-                    uint32_t v[8][16];
+                    uint32_t v[4 * kTokPerWait][16];
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         if (c < hp16) tmem_ld16(col + 16 * c, v[c]);
-                    if (two) {
+                    if constexpr (kTokPerWait == 2) {
+                        if (two) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < hp16) tmem_ld16(col + p.HP + 16 * c, v[4 + c]);
+                            for (int c = 0; c < 4; ++c)
+                                if (c < hp16) tmem_ld16(col + p.HP + 16 * c, v[4 + c]);
+                        }
                     }
                     tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
+                    for (int u = 0; u < kTokPerWait; ++u) {
                         if (u == 1 && !two) break;
                         const int tk = tok + u;
                         const float4 *wt = sm.w4 + (tk * p.HP >> 2);   // broadcast 16-byte loads
@@ -449,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-size_t score_smem_bytes(int n_pad, int hadamard_q) {
-    return 1024 + (size_t)n_pad * 256 * (hadamard_q ? 2 : 1) + (size_t)kStages * kTileBytes +
+size_t score_smem_bytes(int n_pad, int hadamard_q, int n_stages) {
+    return 1024 + (size_t)n_pad * 256 * (hadamard_q ? 2 : 1) + (size_t)n_stages * kTileBytes +
            sizeof(Smem);
 }
 
@@ -486,19 +501,27 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     const int64_t span = a.fill_masked ? a.ld : (int64_t)b.max_kv;
     const int64_t tiles = (span + kTileKeys - 1) / kTileKeys;
     const int64_t work = tiles * (int64_t)b.B * p.groups_per_seq;
-    int64_t tpc = (work + 4 * 152 - 1) / (4 * 152);
-    tpc = std::max<int64_t>(4, std::min<int64_t>(64, tpc));
+    // About two CTAs' worth of tiles per SM; short chunks (small decode
+    // batches) run with a 2-deep ring so that several CTAs share an SM.
+    int64_t tpc = (work + 2 * 152 - 1) / (2 * 152);
+    tpc = std::max<int64_t>(2, std::min<int64_t>(64, tpc));
     p.tiles_per_cta = (int)tpc;
+    p.stages = tpc <= 2 ? 2 : kMaxStages;
     const int64_t chunks = (tiles + tpc - 1) / tpc;
     const int64_t groups = (int64_t)b.B * p.groups_per_seq;
     if (groups > 65535 || chunks > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
-    const size_t smem = score_smem_bytes(p.NP, p.hadamard_q);
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(score_kernel), 0,
-                                     score_smem_bytes(256, 1) > 232448 ? 232448 : score_smem_bytes(256, 1));
-    if (e != cudaSuccess) return e;
+    const size_t smem = score_smem_bytes(p.NP, p.hadamard_q, p.stages);
+    const size_t smem_max = std::min<size_t>(232448, score_smem_bytes(256, 1, kMaxStages));
     dim3 grid((unsigned)chunks, (unsigned)groups);
-    return launch_k(score_kernel, grid, dim3(kThreads), smem, stream, pdl, p, k_map);
+    if (p.G == 1) {                                    // one token per group: lean decode variant
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(score_kernel<4>), 3, smem_max);
+        if (e != cudaSuccess) return e;
+        return launch_k(score_kernel<4>, grid, dim3(ScoreCfg<4>::kThreads), smem, stream, pdl, p, k_map);
+    }
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(score_kernel<8>), 0, smem_max);
+    if (e != cudaSuccess) return e;
+    return launch_k(score_kernel<8>, grid, dim3(ScoreCfg<8>::kThreads), smem, stream, pdl, p, k_map);
 }
 
 }  // namespace dsa

@@ -1,4 +1,4 @@
-// topk.cu -- exact top-k of each query row of indexer scores.
+// topk.cu -- exact top-k of score rows.
 //
 // ik_llama_opt commit log, "Add GLM-5.2/DeepSeek-V3.2 DSA lightning indexer":
 // the selection is ggml_top_k(min(top_k, n_tokens)) over the causally visible
@@ -6,49 +6,69 @@
 // ascending, so the result is the unique set a full sort by (score desc,
 // position asc) would keep.
 //
-// One CTA per row.  Scores become order-preserving 32-bit keys (-0 folded
-// onto +0).  Three histogram digits (11 + 11 + 10 bits) find the exact key tau
-// of the k-th largest element and the number of keys strictly above it; an
-// ordered compaction then keeps every key > tau plus the first
-// (k - count_above) keys == tau in position order, writing positions in
-// ascending order with warp ballots.
+// Main kernel (topk_cluster_kernel<NT, KPT>): a row is spread over a cluster
+// of C CTAs of NT threads (C = 1..8); cluster thread g = rank * NT + tid
+// holds the order-preserving keys of positions [g * e, (g + 1) * e) in
+// registers, e <= KPT, read from memory once.  Three radix digits (11 + 11 +
+// 10 bits) find the exact key tau of the k-th largest element: each pass
+// counts the digit of the keys that still match the prefix into a shared
+// histogram; in a cluster every CTA adds its counts into the histograms of
+// all CTAs through distributed shared memory, so each finds the same bin
+// after one cluster barrier.  The ordered compaction is one scan: per-thread
+// counts of (key > tau, key == tau) are scanned within the CTA, CTA totals
+// across the cluster, selected positions are staged in shared memory in
+// output order and copied out coalesced.  Output order is position order
+// because the cluster threads hold the row in order.
 //
-// Rows that fit are read once from global memory into shared memory and every
-// pass runs there.  Longer rows take one global histogram pass for the first
-// digit, copy only the keys of the threshold bin into shared memory for the
-// other two digits, and finish with one global compaction pass.
+// Rows longer than 8 * 512 * 32 keys fall back to topk_kernel (one CTA per
+// row, keys staged in shared memory, see topk_impl.cuh).
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
+#include "topk_impl.cuh"
+
+#include <algorithm>
 
 namespace dsa {
 
 namespace {
 constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kSmemCapMax = 49152;   // keys held in shared memory (192 KB)
+constexpr int kMaxCluster = 8;
+constexpr int kSmemCapMax = 49152;   // keys held in shared memory by the fallback (192 KB)
 constexpr int kSmemCapHybrid = 16384;
 
-struct TopkSmem {
-    uint32_t hist[2048];
-    uint32_t warp_sum[kTopkWarps];
-    uint32_t gt[kTopkWarps];
-    uint32_t eq[kTopkWarps];
-    uint32_t sel_bin;
-    uint32_t sel_above;
-    uint32_t n_cand;
+// The token of row r of a score slab, or -1.
+__device__ __forceinline__ int row_token(const DevBatch &b, const RowMap &rows, int64_t r) {
+    if (!rows.slab) return (int)r;
+    const int seq = (int)(r / rows.J);
+    const int j = rows.j0 + (int)(r % rows.J);
+    if (seq >= b.B) return -1;
+    const int q0 = __ldg(b.cu_q + seq), q1 = __ldg(b.cu_q + seq + 1);
+    if (q0 >= 0 && q1 <= b.T && q1 >= q0 && j < q1 - q0) return q0 + j;   // bad bounds: flagged by the score pass
+    return -1;
+}
+}  // namespace
+
+template <int NT>
+struct ClusterSmem {
+    uint32_t hist[2][2048];          // double-buffered digit histograms (cluster sums)
+    uint32_t local[2048];            // this CTA's counts of a pass, when C > 1
+    uint32_t warp_sum[NT / 32];
+    uint32_t cta_total[kMaxCluster]; // packed (gt, eq) totals of the other CTAs, written remotely
+    uint32_t sel_bin, sel_above;
 };
 
-__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t bin) { atomicAdd(hist + bin, 1u); }
-
-// Bins are ranked from the top.  Finds the bin b* holding the kk-th largest
-// key and the count of keys in bins above it.
-__device__ void find_bin(TopkSmem &sm, int nbins, uint32_t kk) {
-    const int per = nbins / kTopkThreads;               // 4 or 2 bins per thread
+// Bins are ranked from the top.  Finds the bin holding the kk-th largest key
+// of `hist` and the count of keys in the bins above it.  Ends with a CTA
+// barrier after which `hist` may be rewritten.
+template <int NT>
+__device__ __forceinline__ void find_bin(ClusterSmem<NT> &sm, const uint32_t *hist, int nb, uint32_t kk) {
+    constexpr int NW = NT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int hi = nbins - tid * per;                    // this thread covers [hi-per, hi)
+    const int per = nb / NT;
+    const int hi = nb - tid * per;                       // this thread covers bins [hi - per, hi)
     uint32_t local = 0;
-    for (int i = 1; i <= per; ++i) local += sm.hist[hi - i];
-    uint32_t incl = local;                               // inclusive scan, descending bins
+    for (int i = 1; i <= per; ++i) local += hist[hi - i];
+    uint32_t incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -56,13 +76,18 @@ __device__ void find_bin(TopkSmem &sm, int nbins, uint32_t kk) {
     }
     if (lane == 31) sm.warp_sum[warp] = incl;
     __syncthreads();
-    uint32_t before = 0;
-    for (int w = 0; w < warp; ++w) before += sm.warp_sum[w];
-    const uint32_t above = before + incl - local;        // keys in bins above this thread's range
+    uint32_t ws = lane < NW ? sm.warp_sum[lane] : 0u;    // scan of the warp totals, in every warp
+#pragma unroll
+    for (int o = 1; o < NW; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, ws, o);
+        if (lane >= o) ws += v;
+    }
+    const uint32_t wprev = __shfl_sync(0xffffffffu, ws, (warp + 31) & 31);
+    const uint32_t above = (warp > 0 ? wprev : 0u) + incl - local;
     if (above < kk && kk <= above + local) {
         uint32_t acc = above;
         for (int i = 1; i <= per; ++i) {
-            const uint32_t c = sm.hist[hi - i];
+            const uint32_t c = hist[hi - i];
             if (acc + c >= kk) {
                 sm.sel_bin = (uint32_t)(hi - i);
                 sm.sel_above = acc;
@@ -74,223 +99,237 @@ __device__ void find_bin(TopkSmem &sm, int nbins, uint32_t kk) {
     __syncthreads();
 }
 
-__device__ __forceinline__ void clear_hist(TopkSmem &sm, int nb) {
-    for (int i = threadIdx.x; i < nb; i += kTopkThreads) sm.hist[i] = 0;
-}
+template <int NT, int KPT>
+__device__ __forceinline__ void select_cluster(ClusterSmem<NT> &sm, uint32_t *stage, const float *row, int n,
+                                               int k, int32_t *out, int C, uint32_t crank, bool vec) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int GT = C * NT;
+    const int e = ((n + GT - 1) / GT + 3) & ~3;          // keys per thread: a multiple of 4, <= KPT
+    const int s0 = ((int)crank * NT + tid) * e;
+    const int cnt = max(0, min(e, n - s0));
 
-// Histogram of digit (key >> sh) & (nb-1) over the keys whose bits above the
-// digit equal `prefix` (all keys when hsh >= 32).  Keys come from shared
-// memory (`keys`) or from the float row in global memory.
-template <bool kShared>
-__device__ __forceinline__ void digit_hist(TopkSmem &sm, const uint32_t *keys, const float *row, int n,
-                                           int sh, int nb, int hsh, uint32_t prefix) {
-    constexpr int U = kShared ? 1 : 4;                   // loads in flight per thread
-    for (int s0 = threadIdx.x; s0 < n; s0 += U * kTopkThreads) {
-        uint32_t key[U];
+    for (int i = tid; i < 3 * 2048; i += NT) (&sm.hist[0][0])[i] = 0;
+    // Every CTA of the cluster must run, and have cleared its histograms,
+    // before any of them adds into another's: arrive now, wait after the loads.
+    if (C > 1) cluster_arrive();
+
+    // ---- this thread's keys, read once
+    uint32_t key[KPT];
+    if (vec) {
+        // float4 loads: s0 is a multiple of 4 and the row stride a multiple of
+        // 4 floats, so the last vector of a row ends inside the row's stride.
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int s = s0 + u * kTopkThreads;
-            key[u] = s < n ? (kShared ? keys[s] : float_key(__ldg(row + s))) : 0u;
+        for (int q = 0; q < KPT / 4; ++q) {
+            float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (4 * q < cnt) f = __ldcg(reinterpret_cast<const float4 *>(row + s0) + q);
+            key[4 * q + 0] = float_key(f.x);
+            key[4 * q + 1] = float_key(f.y);
+            key[4 * q + 2] = float_key(f.z);
+            key[4 * q + 3] = float_key(f.w);
         }
+    } else {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int s = s0 + u * kTopkThreads;
-            if (s < n && (hsh >= 32 || (key[u] >> hsh) == prefix))
-                hist_add(sm.hist, (key[u] >> sh) & (uint32_t)(nb - 1));
-        }
+        for (int j = 0; j < KPT; ++j) key[j] = j < cnt ? float_key(__ldcg(row + s0 + j)) : 0u;
     }
-}
+    if (C > 1) cluster_wait();
+    else __syncthreads();
 
-// Ordered compaction over positions 0..n-1: keeps keys > tau and the first
-// need_eq keys == tau, writing positions in ascending order to out.
-template <bool kShared>
-__device__ void compact(TopkSmem &sm, const uint32_t *keys, const float *row, int n, uint32_t tau,
-                        uint32_t need_eq, int32_t *out) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
-    const int s_begin = min(n, warp * seg), s_end = min(n, s_begin + seg);
+    // ---- three digits: prefix ends as the exact key tau of the k-th largest.
+    // Pass p sums into hist[p & 1].  In a cluster each CTA counts into
+    // `local` first and then adds its counts into the sums of every CTA,
+    // itself included, so that all of them find the same bin without a second
+    // exchange (forwarding from the summed buffer would echo other CTAs'
+    // counts while they arrive).
+    uint32_t prefix = 0, above = 0, kk = (uint32_t)k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int width = pass == 2 ? 10 : 11;
+        const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = 1 << width;
+        const int hsh = sh + width;                     // bits above the digit (32: none)
+        uint32_t *H = sm.hist[pass & 1];
+        uint32_t *cnt_to = C > 1 ? sm.local : H;
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)
+            if (j < cnt && (hsh >= 32 || (key[j] >> hsh) == prefix))
+                atomicAdd(&cnt_to[(key[j] >> sh) & (uint32_t)(nb - 1)], 1u);
+        __syncthreads();
+        if (C > 1) {
+            const uint32_t h0 = smem_u32(H);
+            for (int i = tid; i < nb; i += NT) {
+                const uint32_t v = sm.local[i];
+                if (v) {
+                    sm.local[i] = 0;                     // ready for the next pass
+                    for (int r = 0; r < C; ++r) dsmem_add_u32(dsmem_map(h0 + 4u * (uint32_t)i, (uint32_t)r), v);
+                }
+            }
+            cluster_sync_all();
+        }
+        find_bin<NT>(sm, H, nb, kk);
+        prefix = (prefix << width) | sm.sel_bin;
+        above += sm.sel_above;
+        kk -= sm.sel_above;
+        if (pass == 0)                                   // hist[0] again serves pass 2
+            for (int i = tid; i < 2048; i += NT) H[i] = 0;
+    }
+
+    // ---- ordered compaction: keep key > tau and the first need_eq keys == tau
+    const uint32_t tau = prefix, need_eq = (uint32_t)k - above;
     uint32_t gt = 0, eq = 0;
-    for (int s0 = s_begin; s0 < s_end; s0 += 32) {
-        const int s = s0 + lane;
-        const bool in = s < s_end;
-        const uint32_t key = in ? (kShared ? keys[s] : float_key(__ldg(row + s))) : 0u;
-        gt += __popc(__ballot_sync(0xffffffffu, in && key > tau));
-        eq += __popc(__ballot_sync(0xffffffffu, in && key == tau));
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        if (j < cnt) {
+            gt += key[j] > tau;
+            eq += key[j] == tau;
+        }
     }
-    if (lane == 0) {
-        sm.gt[warp] = gt;
-        sm.eq[warp] = eq;
+    const uint32_t packed = (gt << 16) | eq;           // a CTA holds at most 16384 keys
+    uint32_t incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) sm.warp_sum[warp] = incl;
+    __syncthreads();
+    uint32_t ws = lane < NW ? sm.warp_sum[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < NW; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, ws, o);
+        if (lane >= o) ws += v;
+    }
+    const uint32_t wprev = __shfl_sync(0xffffffffu, ws, (warp + 31) & 31);
+    const uint32_t total = __shfl_sync(0xffffffffu, ws, NW - 1);
+    const uint32_t before = (warp > 0 ? wprev : 0u) + incl - packed;
+    uint32_t low_gt = 0, low_eq = 0;                     // keys of the lower-ranked CTAs
+    if (C > 1) {
+        if (tid < C && tid > (int)crank)
+            dsmem_st_u32(dsmem_map(smem_u32(&sm.cta_total[crank]), (uint32_t)tid), total);
+        cluster_sync_all();                              // last cluster access
+        for (int r = 0; r < (int)crank; ++r) {
+            low_gt += sm.cta_total[r] >> 16;
+            low_eq += sm.cta_total[r] & 0xFFFFu;
+        }
+    }
+    const uint32_t cta_base = low_gt + min(low_eq, need_eq);          // selected before this CTA
+    const uint32_t cta_sel = (total >> 16) + min(low_eq + (total & 0xFFFFu), need_eq) - min(low_eq, need_eq);
+    uint32_t eq_before = low_eq + (before & 0xFFFFu);
+    uint32_t sel = low_gt + (before >> 16) + min(eq_before, need_eq) - cta_base;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+        if (j < cnt) {
+            const bool is_eq = key[j] == tau;
+            if (key[j] > tau || (is_eq && eq_before < need_eq)) stage[sel++] = (uint32_t)(s0 + j);
+            eq_before += is_eq;
+        }
     }
     __syncthreads();
-    uint32_t gt_before = 0, eq_before = 0;
-    for (int w = 0; w < warp; ++w) {
-        gt_before += sm.gt[w];
-        eq_before += sm.eq[w];
-    }
-    uint32_t sel_before = gt_before + min(eq_before, need_eq);
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int s0 = s_begin; s0 < s_end; s0 += 32) {
-        const int s = s0 + lane;
-        const bool in = s < s_end;
-        const uint32_t key = in ? (kShared ? keys[s] : float_key(__ldg(row + s))) : 0u;
-        const bool is_gt = in && key > tau;
-        const bool is_eq = in && key == tau;
-        const uint32_t eq_ballot = __ballot_sync(0xffffffffu, is_eq);
-        const uint32_t eq_rank = eq_before + __popc(eq_ballot & lt_mask);
-        const bool sel = is_gt || (is_eq && eq_rank < need_eq);
-        const uint32_t sel_ballot = __ballot_sync(0xffffffffu, sel);
-        if (sel) out[sel_before + __popc(sel_ballot & lt_mask)] = s;
-        eq_before += __popc(eq_ballot);
-        sel_before += __popc(sel_ballot);
-    }
+    for (uint32_t i = tid; i < cta_sel; i += NT) out[cta_base + i] = (int32_t)stage[i];
 }
 
-}  // namespace
-
-__device__ __forceinline__ void topk_row(const float *__restrict__ scores, int64_t ld, const DevBatch &b,
-                                         RowMap rows, int k, int32_t *__restrict__ idx, uint32_t *status,
-                                         int cap) {
-    __shared__ TopkSmem sm;
-    extern __shared__ uint32_t keys[];                   // cap keys
-    const int tid = threadIdx.x;
-    const int64_t r = blockIdx.x;
-    int t;
-    if (rows.slab) {
-        const int seq = (int)(r / rows.J);
-        const int j = rows.j0 + (int)(r % rows.J);
-        if (seq >= b.B) return;
-        const int q0 = __ldg(b.cu_q + seq), q1 = __ldg(b.cu_q + seq + 1);
-        if (q0 < 0 || q1 > b.T || q1 < q0) return;     // flagged by the score pass
-        if (j >= q1 - q0) return;
-        t = q0 + j;
-    } else {
-        t = (int)r;
-    }
-    int32_t *out = idx + (int64_t)t * k;
-    const int pos = __ldg(b.q_pos + t);
-    if (pos < 0 || pos >= b.max_kv || (int64_t)pos >= ld) {
-        if (tid == 0) flag(status, DSA_DEV_BAD_POSITION);
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
-        return;
-    }
-    const int n = pos + 1;
-    if (n <= k) {
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
-        return;
-    }
-    pdl_wait();                                          // the scores come from the preceding kernel
-    const float *row = scores + r * ld;
-
-    if (n <= cap) {
-        // ---- whole row in shared memory
-        for (int s0 = tid; s0 < n; s0 += 8 * kTopkThreads) {
-            float f[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int s = s0 + u * kTopkThreads;
-                f[u] = s < n ? __ldg(row + s) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int s = s0 + u * kTopkThreads;
-                if (s < n) keys[s] = float_key(f[u]);
-            }
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT) topk_cluster_kernel(const float *__restrict__ scores, int64_t ld, DevBatch b,
+                                                          RowMap rows, int k, int32_t *__restrict__ idx,
+                                                          uint32_t *status, int C, int vec) {
+    __shared__ ClusterSmem<NT> sm;
+    extern __shared__ uint32_t stage[];                 // min(k, NT * KPT) selected positions
+    tl_start(b.timeline, kTlTopk);
+    const uint32_t crank = C > 1 ? cluster_rank() : 0u;
+    const int64_t r = blockIdx.x / C;
+    const int t = row_token(b, rows, r);               // uniform over the cluster
+    if (t >= 0) {
+        int32_t *out = idx + (int64_t)t * k;
+        const int pos = __ldg(b.q_pos + t);
+        const int g = (int)crank * NT + (int)threadIdx.x, GT = C * NT;
+        if (pos < 0 || pos >= b.max_kv || (int64_t)pos >= ld) {
+            if (g == 0) flag(status, DSA_DEV_BAD_POSITION);
+            for (int i = g; i < k; i += GT) out[i] = -1;
+        } else if (pos + 1 <= k) {
+            for (int i = g; i < k; i += GT) out[i] = i <= pos ? i : -1;
+        } else {
+            pdl_wait();                                // the scores come from the preceding kernel
+            select_cluster<NT, KPT>(sm, stage, scores + r * ld, pos + 1, k, out, C, crank, vec != 0);
         }
-        clear_hist(sm, 2048);
-        __syncthreads();
-        uint32_t prefix = 0, above = 0, kk = (uint32_t)k;
-        const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-#pragma unroll
-        for (int pass = 0; pass < 3; ++pass) {
-            const int nb = 1 << widths[pass];
-            if (pass > 0) {
-                clear_hist(sm, nb);
-                __syncthreads();
-            }
-            digit_hist<true>(sm, keys, row, n, shifts[pass], nb, shifts[pass] + widths[pass], prefix);
-            __syncthreads();
-            find_bin(sm, nb, kk);
-            prefix = (prefix << widths[pass]) | sm.sel_bin;
-            above += sm.sel_above;
-            kk -= sm.sel_above;
-            __syncthreads();
-        }
-        compact<true>(sm, keys, row, n, prefix, (uint32_t)k - above, out);
-        return;
     }
-
-    // ---- long row: first digit from global memory
-    clear_hist(sm, 2048);
-    if (tid == 0) sm.n_cand = 0;
     __syncthreads();
-    digit_hist<false>(sm, keys, row, n, 21, 2048, 32, 0);
-    __syncthreads();
-    find_bin(sm, 2048, (uint32_t)k);
-    const uint32_t b1 = sm.sel_bin;
-    uint32_t above = sm.sel_above;
-    uint32_t kk = (uint32_t)k - above;
-    const uint32_t c1 = sm.hist[b1];
-    __syncthreads();
-    uint32_t prefix = b1;
-    if ((int)c1 <= cap) {
-        // copy the threshold bin's keys, refine the two lower digits there
-        for (int s0 = tid; s0 < n; s0 += 4 * kTopkThreads) {
-            uint32_t key[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s = s0 + u * kTopkThreads;
-                key[u] = s < n ? float_key(__ldg(row + s)) : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s = s0 + u * kTopkThreads;
-                if (s < n && (key[u] >> 21) == b1) keys[atomicAdd(&sm.n_cand, 1u)] = key[u];
-            }
-        }
-        __syncthreads();
-        const int nc = (int)sm.n_cand;
-        const int shifts[2] = {10, 0}, widths[2] = {11, 10};
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int nb = 1 << widths[pass];
-            clear_hist(sm, nb);
-            __syncthreads();
-            digit_hist<true>(sm, keys, row, nc, shifts[pass], nb, shifts[pass] + widths[pass], prefix);
-            __syncthreads();
-            find_bin(sm, nb, kk);
-            prefix = (prefix << widths[pass]) | sm.sel_bin;
-            above += sm.sel_above;
-            kk -= sm.sel_above;
-            __syncthreads();
-        }
-    } else {
-        const int shifts[2] = {10, 0}, widths[2] = {11, 10};
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int nb = 1 << widths[pass];
-            clear_hist(sm, nb);
-            __syncthreads();
-            digit_hist<false>(sm, keys, row, n, shifts[pass], nb, shifts[pass] + widths[pass], prefix);
-            __syncthreads();
-            find_bin(sm, nb, kk);
-            prefix = (prefix << widths[pass]) | sm.sel_bin;
-            above += sm.sel_above;
-            kk -= sm.sel_above;
-            __syncthreads();
-        }
-    }
-    compact<false>(sm, keys, row, n, prefix, (uint32_t)k - above, out);
+    pdl_trigger();   // late: waiting dependents would share the SMs
+    tl_end(b.timeline, kTlTopk);
 }
 
+// Fallback for rows longer than a cluster holds in registers.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restrict__ scores, int64_t ld,
                                                             DevBatch b, RowMap rows, int k,
                                                             int32_t *__restrict__ idx, uint32_t *status,
                                                             int cap) {
+    __shared__ topk::Shared<kTopkThreads> sm;
+    extern __shared__ uint32_t keys[];                   // cap keys
     tl_start(b.timeline, kTlTopk);
-    topk_row(scores, ld, b, rows, k, idx, status, cap);
+    const int tid = threadIdx.x;
+    const int64_t r = blockIdx.x;
+    const int t = row_token(b, rows, r);
+    if (t >= 0) {
+        int32_t *out = idx + (int64_t)t * k;
+        const int pos = __ldg(b.q_pos + t);
+        if (pos < 0 || pos >= b.max_kv || (int64_t)pos >= ld) {
+            if (tid == 0) flag(status, DSA_DEV_BAD_POSITION);
+            for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
+        } else if (pos + 1 <= k) {
+            for (int i = tid; i < k; i += kTopkThreads) out[i] = i <= pos ? i : -1;
+        } else {
+            pdl_wait();
+            topk::select_row<kTopkThreads, -1>(sm, tid, keys, cap, scores + r * ld, pos + 1, k, out, nullptr);
+        }
+    }
     __syncthreads();
-    pdl_trigger();   // late: waiting dependents would share the SMs
+    pdl_trigger();
     tl_end(b.timeline, kTlTopk);
+}
+
+namespace {
+
+template <int NT, int KPT>
+cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k, int32_t *idx,
+                           uint32_t *status, cudaStream_t stream, bool pdl, int64_t nrows, int C, int vec) {
+    if (nrows * C > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const size_t stage = (size_t)std::min(k, NT * KPT) * 4;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_cluster_kernel<NT, KPT>),
+                                     NT == 256 ? 4 : (KPT == 16 ? 5 : 6), (size_t)NT * KPT * 4);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nrows * C));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = stage;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = C > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<NT, KPT>, scores, ld, b, rows, k, idx, status, C, vec);
+}
+
+}  // namespace
+
+// Explicit configuration (threads per CTA, keys per thread, cluster size);
+// nt * kpt * C must cover the longest row.
+cudaError_t launch_topk_cfg(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k, int32_t *idx,
+                            uint32_t *status, cudaStream_t stream, bool pdl, int nt, int kpt, int C) {
+    const int64_t nrows = rows.slab ? (int64_t)b.B * rows.J : (int64_t)b.T;
+    if (nrows <= 0) return cudaSuccess;
+    if (C < 1 || C > kMaxCluster || (int64_t)nt * kpt * C < b.max_kv) return cudaErrorInvalidValue;
+    const int vec = (ld % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0) ? 1 : 0;
+    if (nt == 512 && kpt == 16)
+        return launch_cluster<512, 16>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec);
+    if (nt == 512 && kpt == 32)
+        return launch_cluster<512, 32>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec);
+    if (nt == 256 && kpt == 32)
+        return launch_cluster<256, 32>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k,
@@ -298,12 +337,23 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
     const int64_t nrows = rows.slab ? (int64_t)b.B * rows.J : (int64_t)b.T;
     if (nrows <= 0) return cudaSuccess;
     if (nrows > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    int cap = b.max_kv <= kSmemCapMax ? b.max_kv : kSmemCapHybrid;
-    cap = (cap + 3) & ~3;
-    if (b.max_kv <= k) cap = 0;                          // every row is returned whole
+    const int64_t n_max = b.max_kv;                      // no row is longer
+    // Rows up to 8192 keys: one CTA per row -- 256 threads (several CTAs per
+    // SM) when rows are plentiful, 512 when latency matters.  Longer rows:
+    // 512 x 32 keys per CTA in clusters of up to 8 CTAs (measured on GB300:
+    // 4 x 16384 beats 8 x 8192 for 64k-key rows; clusters never pay for
+    // 8192-key rows).
+    if (n_max <= 8192) {
+        if (nrows >= 2 * kSMs)
+            return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 256, 32, 1);
+        return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 16, 1);
+    }
+    if (n_max <= (int64_t)kMaxCluster * 512 * 32)
+        return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 32,
+                               (int)((n_max + 512 * 32 - 1) / (512 * 32)));
+    int cap = kSmemCapHybrid;
     const size_t smem = (size_t)cap * 4;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_kernel), 2,
-                                     (size_t)kSmemCapMax * 4);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_kernel), 2, (size_t)kSmemCapMax * 4);
     if (e != cudaSuccess) return e;
     return launch_k(topk_kernel, dim3((unsigned)nrows), dim3(kTopkThreads), smem, stream, pdl, scores, ld, b,
                     rows, k, idx, status, cap);

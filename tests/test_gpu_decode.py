@@ -118,3 +118,60 @@ def test_multi_sequence_prefill_chunks(dsa):
     wl = S.Workload("mixed", 51, kv_len=[700, 3000], q_pos=[680 + i for i in range(20)] + [2990 + i for i in range(10)],
                     cu_q=[0, 20, 30], H_I=64, H=64, top_k=512, hadamard=True)
     check_workload(dsa, wl)
+
+
+def _decode_on(dsa, wl, inp, b, ws, kc, kv):
+    import torch
+    out = torch.full((wl.T, wl.H, 512), float("nan"), device="cuda")
+    lse = torch.full((wl.T, wl.H), float("nan"), device="cuda")
+    idx = torch.full((wl.T, wl.top_k), -7, dtype=torch.int32, device="cuda")
+    dsa.dsa_decode(to_dev(inp.k_new), to_dev(inp.q_idx), to_dev(inp.w), to_dev(inp.q_lat), to_dev(inp.q_rope),
+                   kc, kv, b, wl.top_k, wl.sm_scale, wl.hadamard, out, lse, idx, ws)
+    status = dsa.dsa_read_device_status(ws)
+    return dict(idx=idx.cpu().numpy(), out=out.cpu().numpy(), lse=lse.cpu().numpy(), status=status)
+
+
+def test_decode_steps_reuse_workspace(dsa):
+    """Consecutive single-token steps on one workspace.  Decode batches select
+    inside the score kernel with per-sequence histograms and counters kept in
+    the workspace; they must be back at zero after every call.  The rows cover
+    n < k, n == k, n == k + 1, rows that fit the kernel's shared-memory key
+    scratch and rows longer than it, and sequences scored by one CTA and by
+    many."""
+    kv_len = [40000, 3000, 2049, 70000, 200]
+    steps = [[38990, 1000, 2046, 68990, 10],
+             [38991, 1001, 2047, 68991, 11],
+             [38992, 2999, 2048, 69999, 199]]
+    wl0 = S.Workload("decode_steps", 61, kv_len=kv_len, q_pos=steps[0], cu_q=list(range(6)),
+                     H_I=32, H=16, top_k=2048)
+    inp = S.make_inputs(wl0)
+    max_kv = max(kv_len)
+    batches = [dsa.Batch.from_host(wl0.cu_q, q, wl0.kv_off, wl0.cache_rows, max_q_per_seq=1, max_kv=max_kv)
+               for q in steps]
+    ws = dsa.workspace(dsa.DSA_OP_DECODE, batches[0], wl0.H_I, wl0.H, wl0.top_k)
+    kc, kv = to_dev(inp.k_cache), to_dev(inp.kv_cache)
+    kc_ref = inp.k_cache.copy()
+    for q, b in zip(steps, batches):
+        wl = S.Workload("decode_steps", 61, kv_len=kv_len, q_pos=q, cu_q=wl0.cu_q, H_I=32, H=16, top_k=2048)
+        g = _decode_on(dsa, wl, inp, b, ws, kc, kv)
+        assert g["status"] == 0
+        oracle.k_append(inp.k_new, oracle.Batch.of(wl), kc_ref, False)
+        assert np.array_equal(kc.cpu().numpy().view(np.uint16), kc_ref.view(np.uint16))
+        check_rows(wl, inp, g, list(range(wl.T)), kc_ref)
+
+
+def test_decode_all_scores_tied(dsa):
+    """Zero indexer weights make every visible score 0: the selection must be
+    the k lowest positions, for rows held in shared memory and for rows so
+    long that the threshold bin itself exceeds the shared-memory scratch."""
+    wl = S.Workload("decode_ties", 62, kv_len=[70000, 5000, 1000], q_pos=[69999, 4999, 999],
+                    cu_q=[0, 1, 2, 3], H_I=16, H=8, top_k=2048)
+    inp = S.make_inputs(wl)
+    inp.w[:] = 0.0
+    b = dev_batch(wl)
+    ws = dsa.workspace(dsa.DSA_OP_DECODE, b, wl.H_I, wl.H, wl.top_k)
+    g = _decode_on(dsa, wl, inp, b, ws, to_dev(inp.k_cache), to_dev(inp.kv_cache))
+    assert g["status"] == 0
+    assert g["idx"][0].tolist() == list(range(2048))
+    assert g["idx"][1].tolist() == list(range(2048))
+    assert g["idx"][2].tolist() == list(range(1000)) + [-1] * 1048

@@ -123,6 +123,13 @@ def _topk_case(kind, rng):
     elif kind == "long_row":
         L, pos = 131072, [131071, 70000]
         s = rng.standard_normal((len(pos), L)).astype(np.float32)
+    elif kind == "cluster3":                    # aligned rows spread over a 3-CTA cluster
+        L, pos = 20000, [19999, 12000, 8191, 8192, 3000, 100]
+        s = rng.standard_normal((len(pos), L)).astype(np.float32)
+        s[:, 5000:5100] = 0.5                   # a run of ties inside one CTA's share
+    elif kind == "beyond_cluster":              # longer than a cluster holds: shared-memory path
+        L, pos = 140000, [139999, 131072]
+        s = rng.standard_normal((len(pos), L)).astype(np.float32)
     elif kind == "narrow":                      # distinct values that share high bits
         L, pos = 9000, [8999]
         s = (1.0 + rng.integers(0, 1 << 12, (1, L)) * 2.0 ** -23).astype(np.float32)
@@ -131,7 +138,8 @@ def _topk_case(kind, rng):
     return s, pos
 
 
-@pytest.mark.parametrize("kind", ["random", "ties", "all_equal", "signed_zero", "neg_inf", "long_row", "narrow"])
+@pytest.mark.parametrize("kind", ["random", "ties", "all_equal", "signed_zero", "neg_inf", "long_row", "narrow",
+                                  "cluster3", "beyond_cluster"])
 @pytest.mark.parametrize("k", [1, 2048])
 def test_topk_bit_exact_on_oracle_scores(dsa, kind, k):
     import torch
