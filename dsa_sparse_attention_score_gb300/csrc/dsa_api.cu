@@ -14,10 +14,6 @@ namespace {
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr size_t kAlign = 256;
 constexpr int64_t kSlabBytes = int64_t(1) << 30;  // score slab budget in the workspace
-// Reduce the split-KV partials of a token inside a thread-block cluster
-// (distributed shared memory) instead of through the workspace and a combine
-// kernel.  Off: measured slower on GB300 with scalar remote stores.
-constexpr bool kClusterReduce = false;
 
 cudaEvent_t *g_trace = nullptr;
 int g_trace_n = 0;
@@ -98,10 +94,13 @@ struct Layout {
     int n_split = 1, tiles_per_cta = 1;
 };
 
+// Splits of a token's selected rows across CTAs: with fewer tokens than SMs,
+// up to one wave of CTAs (one per SM), each keeping at least two tiles so
+// that its gathers overlap its arithmetic.
 void attn_split(int T, int k, int *n_split, int *tpc) {
-    const int n_tiles = (k + 127) / 128;
+    const int n_tiles = (k + attn_tile_rows() - 1) / attn_tile_rows();
     int ns = 1;
-    if (T < 2 * kSMs) ns = std::min(n_tiles, (2 * kSMs + T - 1) / T);
+    if (T < kSMs) ns = std::max(1, std::min(n_tiles / 2, kSMs / T));
     int t = (n_tiles + ns - 1) / ns;
     ns = (n_tiles + t - 1) / t;
     *n_split = ns;
@@ -182,7 +181,6 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
     a.lse = lse;
     a.n_split = L.n_split;
     a.tiles_per_cta = L.tiles_per_cta;
-    a.clustered = kClusterReduce && L.n_split > 1 && attn_cluster_ok(L.n_split);
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     a.part_o = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_o) : nullptr;
     a.part_ml = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_ml) : nullptr;
@@ -260,7 +258,7 @@ dsa_status_t dsa_decode_launches(const dsa_batch_t *batch, int H_I, int H, int k
     if (k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
     const Layout L = layout(DSA_OP_DECODE, batch, k);
     const int slabs = (batch->max_q_per_seq + L.J - 1) / L.J;
-    const bool combine = L.n_split > 1 && !(kClusterReduce && attn_cluster_ok(L.n_split));
+    const bool combine = L.n_split > 1;
     *launches = (batch->max_q_per_seq == 1 ? 0 : 1) + 2 * slabs + 1 + (combine ? 1 : 0);
     return DSA_OK;
 }

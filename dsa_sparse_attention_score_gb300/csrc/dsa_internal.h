@@ -91,25 +91,23 @@ struct AttnLaunch {
     const int32_t *idx;      // [T, k]
     float *out;              // [T, H, 512]
     float *lse;              // [T, H] or null
-    int tiles_per_cta;       // 128-row tiles handled by one CTA
+    int tiles_per_cta;       // attention row tiles handled by one CTA
     int n_split;             // CTAs per (token, head group)
     float *part_o;           // [T, n_split, groups*64, 512] when n_split > 1
     float *part_ml;          // [T, n_split, groups*64, 2]
-    int clustered;           // reduce the splits of a token inside a thread-block cluster
 };
 cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map,
                                const CUtensorMap &q_rope_map, const CUtensorMap &kv_map,
                                const DevBatch &b, uint32_t *status, cudaStream_t stream, bool pdl);
 cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream, bool pdl);
 
-// Sets a kernel's dynamic shared-memory limit once per device.
 // Sets a kernel's dynamic shared-memory limit once per device; `slot`
 // (0..kSmemAttrSlots-1) names the kernel instance.
 constexpr int kSmemAttrSlots = 8;
 cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes);
 
-// Whether a token's n_split attention CTAs can run as one cluster here.
-bool attn_cluster_ok(int n_split);
+// Rows of one attention tile (the unit of the split across CTAs).
+int attn_tile_rows();
 
 // Shared-memory bytes of the attention kernel (for the host's occupancy set-up).
 size_t sparse_attn_smem_bytes();
