@@ -81,6 +81,8 @@ struct Ctl {
     float red[4][kHeads];
     float m[kHeads];
     float alpha[kHeads];
+    float2 ma[kHeads];       // (m, alpha) of the current tile, read together
+    int32_t resc[2];         // any head of warp 0 / 1 rescaled in this tile
     float l[kHeads];
     int32_t warp_alive[4];
 };
@@ -342,20 +344,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ctl.m[h] = mn;
                 ctl.alpha[h] = al;
+                ctl.ma[h] = make_float2(mn, al);
+                const bool any = __any_sync(0xffffffffu, al != 1.f);
+                if (lane == 0) ctl.resc[warp] = any ? 1 : 0;
             }
             named_barrier(1, 128);
-            bool rescale = false;      // identical in every thread: all read the same alphas
-#pragma unroll
-            for (int h = 0; h < kHeads; ++h) rescale |= ctl.alpha[h] != 1.f;
+            const bool rescale = ctl.resc[0] | ctl.resc[1];   // identical in every thread
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 const int h = hb + j;
-                const float mh0 = ctl.m[h], mh1 = ctl.m[h + 1];
-                const float p0 = (mh0 == -INFINITY) ? 0.f : exp2f(x[j] - mh0);
-                const float p1 = (mh1 == -INFINITY) ? 0.f : exp2f(x[j + 1] - mh1);
-                lpart[j] = lpart[j] * ctl.alpha[h] + p0;
-                lpart[j + 1] = lpart[j + 1] * ctl.alpha[h + 1] + p1;
+                const float2 a0 = ctl.ma[h], a1 = ctl.ma[h + 1];
+                const float p0 = (a0.x == -INFINITY) ? 0.f : exp2f(x[j] - a0.x);
+                const float p1 = (a1.x == -INFINITY) ? 0.f : exp2f(x[j + 1] - a1.x);
+                lpart[j] = lpart[j] * a0.y + p0;
+                lpart[j + 1] = lpart[j + 1] * a1.y + p1;
                 const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
                 pk[j / 2] = *reinterpret_cast<const uint32_t *>(&pb);
             }
