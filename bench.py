@@ -38,9 +38,9 @@ METRIC = "DSA decode tok/s & prefill tok/s on 1 GB300; % of HBM / tensor rooflin
 UNIT = "tok/s"
 WORKLOADS = {"tiny_decode": 1, "batched_decode": 2, "ragged_decode": 3, "prefill_chunk": 4, "long_prefill": 5}
 STAGES = ["k_append", "indexer_score", "topk", "sparse_attn", "attn_combine"]
-KERNEL_OF_STAGE = {"k_append": "k_append_kernel", "indexer_score": "score_kernel", "topk": "topk_kernel",
+KERNEL_OF_STAGE = {"k_append": "k_append_kernel", "indexer_score": "score_kernel", "topk": "topk_cluster_kernel",
                    "sparse_attn": "sparse_attn_kernel", "attn_combine": "attn_combine_kernel"}
-SOURCE_OF_KERNEL = {"k_append_kernel": "k_append.cu", "score_kernel": "score.cu", "topk_kernel": "topk.cu",
+SOURCE_OF_KERNEL = {"k_append_kernel": "k_append.cu", "score_kernel": "score.cu", "topk_cluster_kernel": "topk.cu",
                     "sparse_attn_kernel": "sparse_attn.cu", "attn_combine_kernel": "sparse_attn.cu"}
 
 
