@@ -413,16 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tx < kHeads) ctl.l[tx] = ctl.red[0][tx] + ctl.red[1][tx] + ctl.red[2][tx] + ctl.red[3][tx];
         if (lane == 0) ctl.warp_alive[sw] = alive ? 1 : 0;
         named_barrier(1, 128);
-        if (alive) {
-            // Stage this CTA's [head][dim] block in the dead tile buffers (all
-            // gathers and MMAs are done) and write it with bulk copies:
-            // unnormalised partials when the token is split, the normalised
+        const bool all_alive = ctl.warp_alive[0] && ctl.warp_alive[1] && ctl.warp_alive[2] && ctl.warp_alive[3];
+        if (all_alive) {
+            // This CTA's [head][dim] block straight from TMEM: thread (quarter,
+            // lane) holds output dim c*128 + quarter*32 + lane of every head,
+            // so each store instruction of a warp writes 128 contiguous bytes.
+            // Unnormalised partials when the token is split, the normalised
             // output otherwise.
             tc_fence_after();
             const int H = p.H;
             const int rows = p.n_split > 1 ? kHeads : H;
-            const int rd = quarter * 32 + lane;            // output dim within a 128-dim chunk
-            float *stage = reinterpret_cast<float *>(c_s);
+            float *dst = p.n_split > 1 ? p.part_o + ((int64_t)t * p.n_split + split) * kHeads * D_L
+                                       : p.out + (int64_t)t * H * D_L;
+            const int rd = quarter * 32 + lane;
             for (int c = 0; c < 4; ++c) {
                 const int d = c * 128 + rd;
 #pragma unroll
@@ -431,32 +434,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem + lane_addr + kColO + c * kHeads + half * 32, u);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int h = half * 32 + j;
-                        float o = __uint_as_float(u[j]);
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int h = half * 32 + jj;
+                        float o = __uint_as_float(u[jj]);
                         if (p.n_split == 1) {
                             const float l = ctl.l[h];
                             o = l > 0.f ? o / l : 0.f;
                         }
-                        if (h < rows) stage[h * D_L + d] = o;
+                        if (h < rows) dst[h * D_L + d] = o;
                     }
                 }
-            }
-            fence_proxy_async_smem();
-        }
-        named_barrier(1, 128);                       // every warp, whatever its state
-        const bool all_alive = ctl.warp_alive[0] && ctl.warp_alive[1] && ctl.warp_alive[2] && ctl.warp_alive[3];
-        if (all_alive) {
-            const int H = p.H;
-            const int rows = p.n_split > 1 ? kHeads : H;
-            if (tx == 0) {
-                float *dst = p.n_split > 1 ? p.part_o + ((int64_t)t * p.n_split + split) * kHeads * D_L
-                                           : p.out + (int64_t)t * H * D_L;
-                const uint32_t bytes = (uint32_t)(rows * D_L * 4);
-                for (uint32_t off = 0; off < bytes; off += 32768)
-                    bulk_s2g(reinterpret_cast<uint8_t *>(dst) + off, smem_u32(c_s) + off, min(32768u, bytes - off));
-                bulk_commit();
-                bulk_wait_all();
             }
             if (tx < kHeads) {
                 const int h = tx;
