@@ -403,6 +403,8 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
         a.k_dtype = k_dtype;
         a.k_cache = k_cache;
         a.hadamard_k = hadamard != 0;
+        // decode: the top-k that follows runs one small CTA group per sequence
+        a.early_ok = fuse_append && (int64_t)batch->batch * ((batch->max_kv + 8191) / 8192) <= kSMs / 4;
         if (j0 == 0) trace(1, stream);
         DSA_TRY_CUDA(launch_score(a, km, db, st, stream, !(fuse_append && j0 == 0)));
         if (j0 == 0) trace(2, stream);

@@ -78,6 +78,9 @@ struct ScoreLaunch {
     int k_dtype;
     uint16_t *k_cache;       // written at the token's row
     int hadamard_k;
+    // The kernel that follows is small: when this grid also fits in one wave,
+    // trigger dependents at the start so that they fill the idle SMs.
+    int early_ok;
 };
 cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const DevBatch &b,
                          uint32_t *status, cudaStream_t stream, bool pdl);

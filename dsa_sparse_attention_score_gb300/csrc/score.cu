@@ -59,6 +59,7 @@ struct ScoreParams {
     int hadamard_k;
     int tiles_per_cta;
     int stages;
+    int early;                // trigger dependents at the start (see launch_score)
     int groups_per_seq;
     uint32_t tmem_cols;
 };
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi == 8 ? 1 : 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DevBatch &b = p.b;
     tl_start(b.timeline, kTlScore);
+    if (p.early) pdl_trigger();
 
     // ---- which tokens and keys this CTA covers (uniform across the CTA)
     const int seq = blockIdx.y / p.groups_per_seq;
@@ -456,7 +458,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi == 8 ? 1 : 2)
 
     tc_fence_before();
     __syncthreads();
-    pdl_trigger();   // late: waiting dependents would share the SMs
+    if (!p.early) pdl_trigger();   // late: waiting dependents would share the SMs
     tl_end(b.timeline, kTlScore);
     if (warp == 1) {
         tc_fence_after();
@@ -514,6 +516,9 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     const size_t smem = score_smem_bytes(p.NP, p.hadamard_q, p.stages);
     const size_t smem_max = std::min<size_t>(232448, score_smem_bytes(256, 1, kMaxStages));
     dim3 grid((unsigned)chunks, (unsigned)groups);
+    // One wave of this kernel (decode variant: two CTAs per SM) followed by a
+    // small dependent grid: that grid can start on the SMs left free.
+    p.early = (a.early_ok && p.G == 1 && chunks * groups <= 2 * kSMs) ? 1 : 0;
     if (p.G == 1) {                                    // one token per group: lean decode variant
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(score_kernel<4>), 3, smem_max);
         if (e != cudaSuccess) return e;

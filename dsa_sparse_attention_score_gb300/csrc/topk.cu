@@ -231,10 +231,14 @@ __device__ __forceinline__ void select_cluster(ClusterSmem<NT> &sm, uint32_t *st
 template <int NT, int KPT>
 __global__ void __launch_bounds__(NT) topk_cluster_kernel(const float *__restrict__ scores, int64_t ld, DevBatch b,
                                                           RowMap rows, int k, int32_t *__restrict__ idx,
-                                                          uint32_t *status, int C, int vec) {
+                                                          uint32_t *status, int C, int vec, int early) {
     __shared__ ClusterSmem<NT> sm;
     extern __shared__ uint32_t stage[];                 // min(k, NT * KPT) selected positions
     tl_start(b.timeline, kTlTopk);
+    // A grid of a few CTAs leaves most SMs idle: let the dependent kernel
+    // start its prologue there right away.  A larger one triggers at its
+    // end, since waiting dependents would share its SMs.
+    if (early) pdl_trigger();
     const uint32_t crank = C > 1 ? cluster_rank() : 0u;
     const int64_t r = blockIdx.x / C;
     const int t = row_token(b, rows, r);               // uniform over the cluster
@@ -253,7 +257,7 @@ __global__ void __launch_bounds__(NT) topk_cluster_kernel(const float *__restric
         }
     }
     __syncthreads();
-    pdl_trigger();   // late: waiting dependents would share the SMs
+    if (!early) pdl_trigger();
     tl_end(b.timeline, kTlTopk);
 }
 
@@ -310,7 +314,8 @@ cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, R
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = C > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<NT, KPT>, scores, ld, b, rows, k, idx, status, C, vec);
+    const int early = nrows * C <= kSMs / 4 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<NT, KPT>, scores, ld, b, rows, k, idx, status, C, vec, early);
 }
 
 }  // namespace
