@@ -30,9 +30,11 @@ namespace {
 constexpr int kMaxStages = 4;        // depth of the key-tile ring (runtime: 2..4)
 constexpr int kTileKeys = 128;
 constexpr int kTileBytes = kTileKeys * D_I * 2;  // 32 KB: two 64-column SW128 boxes
-// Epilogue warps per CTA: 8 (two per TMEM lane quarter, splitting a group's
-// tokens, two tokens per TMEM round trip) for multi-token groups; 4 (one
-// token per round trip, fewer registers, several CTAs per SM) for decode.
+// Epilogue warps per CTA: 16 (four per TMEM lane quarter, splitting a
+// group's tokens, one token per TMEM round trip) for multi-token groups --
+// measured on GB300 the epilogue, not the tensor core, bounds prefill
+// scoring, and 16 warps hide its latency better than 8 with two tokens per
+// round trip; 4 (several CTAs per SM) for one-token decode groups.
 template <int kEpi> struct ScoreCfg {
     static constexpr int kEpiWarps = kEpi;
     static constexpr int kThreads = 64 + 32 * kEpi;
@@ -190,7 +192,7 @@ __device__ __forceinline__ uint2 appended_key(const void *k_new, int k_dtype, in
 }  // namespace
 
 template <int kEpi>
-__global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi == 8 ? 1 : 2)
+__global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     score_kernel(const ScoreParams p, const __grid_constant__ CUtensorMap k_map) {
     constexpr int kEpiWarps = ScoreCfg<kEpi>::kEpiWarps;
     constexpr int kTokPerWait = ScoreCfg<kEpi>::kTokPerWait;
@@ -524,9 +526,9 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
         if (e != cudaSuccess) return e;
         return launch_k(score_kernel<4>, grid, dim3(ScoreCfg<4>::kThreads), smem, stream, pdl, p, k_map);
     }
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(score_kernel<8>), 0, smem_max);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(score_kernel<16>), 4, smem_max);
     if (e != cudaSuccess) return e;
-    return launch_k(score_kernel<8>, grid, dim3(ScoreCfg<8>::kThreads), smem, stream, pdl, p, k_map);
+    return launch_k(score_kernel<16>, grid, dim3(ScoreCfg<16>::kThreads), smem, stream, pdl, p, k_map);
 }
 
 }  // namespace dsa
