@@ -137,6 +137,30 @@ def topk(scores, q_pos, k: int) -> np.ndarray:
     return idx
 
 
+def topk_sink(scores, q_pos, k: int, n_sink: int, seq_of_row=None, anchors=None) -> np.ndarray:
+    """Top-k with the attention sink forced in.
+
+    ik_llama_opt commit log, "GLM-5.2 DSA indexer: decode-correct via
+    persistent indexer-K cache" (attention-sink force-inclusion) and "per-
+    sequence attention sink": the first n_sink keys of the query's OWN
+    sequence get a +1e20 boost before the argsort, so they always survive;
+    "UPDATE 6": the sink is anchored on the sequence's first present position.
+    Here the boost is taken as unbounded (+inf, which is what +1e20 becomes
+    next to float32 scores: the boosted scores tie with one another), then the
+    plain selection runs: ties go to the lower position.
+      seq_of_row [T]: sequence of each row (needed with anchors);
+      anchors [B]: first present position of each sequence (default 0).
+    """
+    s = np.array(scores, dtype=np.float64, copy=True)
+    for r in range(s.shape[0]):
+        a = 0 if anchors is None else int(anchors[int(seq_of_row[r])])
+        lo = max(a, 0)
+        hi = min(a + n_sink, int(q_pos[r]) + 1, s.shape[1])
+        if hi > lo:
+            s[r, lo:hi] = np.inf
+    return topk(s, q_pos, k)
+
+
 def sparse_attn(q_lat, q_rope, kv_cache, batch: Batch, idx, sm_scale: float):
     """bf16-bit queries.  Returns (out [T,H,512], lse [T,H]) in float64."""
     ql = _c(q_lat, np.uint16)
