@@ -58,8 +58,11 @@ SIGNATURES = {
     "dsa_indexer_k_append": (_I, [_P, _I, _BP, _P, _I, _P, _SZ, _P]),
     "dsa_indexer_score": (_I, [_P, _P, _P, _BP, _I, _I, _P, _I64, _P, _SZ, _P]),
     "dsa_topk": (_I, [_P, _I64, _BP, _I, _P, _P, _SZ, _P]),
+    "dsa_topk_sink": (_I, [_P, _I64, _BP, _I, _I, _P, _P, _P, _SZ, _P]),
     "dsa_sparse_mla_attn": (_I, [_P, _P, _P, _BP, _P, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "dsa_decode": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _P, _P, _P, _P, _SZ, _P]),
+    "dsa_decode_sink": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _P,
+                             _SZ, _P]),
     "dsa_decode_noalloc": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "dsa_workspace_size": (_I, [_I, _BP, _I, _I, _I, C.POINTER(C.c_size_t)]),
     "dsa_workspace_init": (_I, [_P, _SZ, _P]),
@@ -223,6 +226,18 @@ def dsa_topk(scores, batch: Batch, k: int, idx, ws, stream=None):
                           _stream(stream)), "dsa_topk")
 
 
+def dsa_topk_sink(scores, batch: Batch, k: int, n_sink: int, sink_pos0, idx, ws, stream=None):
+    """dsa_topk with the first n_sink positions of each sequence (from
+    sink_pos0[b], an int32 CUDA tensor [B], or 0 when None) forced in."""
+    import torch
+    _req(scores, torch.float32, "scores")
+    _req(idx, torch.int32, "idx")
+    _req(sink_pos0, torch.int32, "sink_pos0")
+    d = batch.desc()
+    _check(lib().dsa_topk_sink(_ptr(scores), scores.shape[1], C.byref(d), k, n_sink, _ptr(sink_pos0), _ptr(idx),
+                               _ptr(ws), ws.numel(), _stream(stream)), "dsa_topk_sink")
+
+
 def dsa_sparse_mla_attn(q_lat, q_rope, kv_cache, batch: Batch, idx, sm_scale: float, out, lse, ws,
                         stream=None):
     import torch
@@ -257,6 +272,30 @@ def dsa_decode(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch: Batch, 
                             _ptr(kv_cache), C.byref(d), q_idx.shape[1], q_lat.shape[1], k, sm_scale,
                             int(hadamard), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws), ws.numel(),
                             _stream(stream)), "dsa_decode")
+
+
+def dsa_decode_sink(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch: Batch, k: int, sm_scale: float,
+                    hadamard: bool, n_sink: int, sink_pos0, out, lse, idx_out, ws, stream=None):
+    """dsa_decode with the attention sink forced into every selection (see
+    dsa_topk_sink)."""
+    import torch
+    kd = DSA_KEY_F16 if k_new.dtype == torch.float16 else DSA_KEY_F32
+    _req(k_new, torch.float16 if kd == DSA_KEY_F16 else torch.float32, "k_new")
+    _req(q_idx, torch.float16, "q_idx")
+    _req(w, torch.float32, "w")
+    _req(q_lat, torch.bfloat16, "q_lat")
+    _req(q_rope, torch.bfloat16, "q_rope")
+    _req(k_cache, torch.float16, "k_cache")
+    _req(kv_cache, torch.bfloat16, "kv_cache")
+    _req(sink_pos0, torch.int32, "sink_pos0")
+    _req(out, torch.float32, "out")
+    _req(lse, torch.float32, "lse")
+    _req(idx_out, torch.int32, "idx_out")
+    d = batch.desc()
+    _check(lib().dsa_decode_sink(_ptr(k_new), kd, _ptr(q_idx), _ptr(w), _ptr(q_lat), _ptr(q_rope), _ptr(k_cache),
+                                 _ptr(kv_cache), C.byref(d), q_idx.shape[1], q_lat.shape[1], k, sm_scale,
+                                 int(hadamard), n_sink, _ptr(sink_pos0), _ptr(out), _ptr(lse), _ptr(idx_out),
+                                 _ptr(ws), ws.numel(), _stream(stream)), "dsa_decode_sink")
 
 
 def dsa_decode_noalloc(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch: Batch, k: int,

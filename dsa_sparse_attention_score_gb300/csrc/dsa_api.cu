@@ -321,8 +321,9 @@ dsa_status_t dsa_indexer_score(const dsa_f16 *q_idx, const float *w, const dsa_f
     return DSA_OK;
 }
 
-dsa_status_t dsa_topk(const float *scores, int64_t ld_scores, const dsa_batch_t *batch, int k,
-                      int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
+static dsa_status_t topk_impl(const float *scores, int64_t ld_scores, const dsa_batch_t *batch, int k,
+                              int n_sink, const int32_t *sink_pos0, int32_t *idx, void *ws, size_t ws_bytes,
+                              cudaStream_t stream) {
     dsa_status_t s = check_batch(batch);
     if (s != DSA_OK) return s;
     if (!scores || !idx) return DSA_ERR_INVALID_ARGUMENT;
@@ -330,9 +331,22 @@ dsa_status_t dsa_topk(const float *scores, int64_t ld_scores, const dsa_batch_t 
     if (ld_scores < batch->max_kv) return DSA_ERR_INVALID_ARGUMENT;
     if (!aligned(scores, 4) || !aligned(idx, 4)) return DSA_ERR_MISALIGNED;
     if ((s = check_ws(ws, ws_bytes, kStatusBytes)) != DSA_OK) return s;
+    if (n_sink < 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (sink_pos0 && !aligned(sink_pos0, 4)) return DSA_ERR_MISALIGNED;
     DSA_TRY_CUDA(launch_topk(scores, ld_scores, dev_batch(batch), RowMap{0, 0, 1}, k, idx,
-                             status_ptr(ws), stream, false));
+                             status_ptr(ws), stream, false, n_sink, sink_pos0));
     return DSA_OK;
+}
+
+dsa_status_t dsa_topk(const float *scores, int64_t ld_scores, const dsa_batch_t *batch, int k,
+                      int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return topk_impl(scores, ld_scores, batch, k, 0, nullptr, idx, ws, ws_bytes, stream);
+}
+
+dsa_status_t dsa_topk_sink(const float *scores, int64_t ld_scores, const dsa_batch_t *batch, int k, int n_sink,
+                           const int32_t *sink_pos0, int32_t *idx, void *ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+    return topk_impl(scores, ld_scores, batch, k, n_sink, sink_pos0, idx, ws, ws_bytes, stream);
 }
 
 dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const dsa_bf16 *kv_cache,
@@ -353,13 +367,15 @@ dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, 
                          false, false);
 }
 
-dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
-                        const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
-                        const dsa_bf16 *kv_cache, const dsa_batch_t *batch, int H_I, int H, int k,
-                        float sm_scale, int hadamard, float *out, float *lse, int32_t *idx_out, void *ws,
-                        size_t ws_bytes, cudaStream_t stream) {
+static dsa_status_t decode_impl(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                                const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
+                                const dsa_bf16 *kv_cache, const dsa_batch_t *batch, int H_I, int H, int k,
+                                float sm_scale, int hadamard, int n_sink, const int32_t *sink_pos0, float *out,
+                                float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream) {
     dsa_status_t s = check_batch(batch);
     if (s != DSA_OK) return s;
+    if (n_sink < 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (sink_pos0 && !aligned(sink_pos0, 4)) return DSA_ERR_MISALIGNED;
     if (!k_new || !q_idx || !w || !q_lat || !q_rope || !k_cache || !kv_cache || !out)
         return DSA_ERR_INVALID_ARGUMENT;
     if (k_dtype != DSA_KEY_F32 && k_dtype != DSA_KEY_F16) return DSA_ERR_INVALID_ARGUMENT;
@@ -408,13 +424,31 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
         if (j0 == 0) trace(1, stream);
         DSA_TRY_CUDA(launch_score(a, km, db, st, stream, !(fuse_append && j0 == 0)));
         if (j0 == 0) trace(2, stream);
-        DSA_TRY_CUDA(launch_topk(slab, L.ld, db, a.rows, k, idx, st, stream, true));
+        DSA_TRY_CUDA(launch_topk(slab, L.ld, db, a.rows, k, idx, st, stream, true, n_sink, sink_pos0));
     }
     trace(3, stream);
     s = run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream, true, true);
     if (L.n_split <= 1) trace(4, stream);
     trace(5, stream);
     return s;
+}
+
+dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                        const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
+                        const dsa_bf16 *kv_cache, const dsa_batch_t *batch, int H_I, int H, int k,
+                        float sm_scale, int hadamard, float *out, float *lse, int32_t *idx_out, void *ws,
+                        size_t ws_bytes, cudaStream_t stream) {
+    return decode_impl(k_new, k_dtype, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch, H_I, H, k, sm_scale,
+                       hadamard, 0, nullptr, out, lse, idx_out, ws, ws_bytes, stream);
+}
+
+dsa_status_t dsa_decode_sink(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                             const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
+                             const dsa_bf16 *kv_cache, const dsa_batch_t *batch, int H_I, int H, int k,
+                             float sm_scale, int hadamard, int n_sink, const int32_t *sink_pos0, float *out,
+                             float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return decode_impl(k_new, k_dtype, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch, H_I, H, k, sm_scale,
+                       hadamard, n_sink, sink_pos0, out, lse, idx_out, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -85,8 +85,11 @@ struct ScoreLaunch {
 cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const DevBatch &b,
                          uint32_t *status, cudaStream_t stream, bool pdl);
 
+// n_sink > 0: the positions [a, a + n_sink) of each row's sequence are forced
+// in, a = sink_pos0[seq] (device, [B]) or 0 when sink_pos0 is null.
 cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k,
-                        int32_t *idx, uint32_t *status, cudaStream_t stream, bool pdl);
+                        int32_t *idx, uint32_t *status, cudaStream_t stream, bool pdl, int n_sink = 0,
+                        const int32_t *sink_pos0 = nullptr);
 
 struct AttnLaunch {
     int H, k;

@@ -46,6 +46,17 @@ __device__ __forceinline__ int row_token(const DevBatch &b, const RowMap &rows, 
     if (q0 >= 0 && q1 <= b.T && q1 >= q0 && j < q1 - q0) return q0 + j;   // bad bounds: flagged by the score pass
     return -1;
 }
+// Forced-in (attention-sink) positions of row r: [a, a + n_sink), a being the
+// sequence's first present position (sink_pos0[seq], or 0 when not given).
+__device__ __forceinline__ void row_sink(const DevBatch &b, const RowMap &rows, int64_t r, int t, int n_sink,
+                                         const int32_t *sink_pos0, int &lo, int &hi) {
+    lo = hi = 0;
+    if (n_sink <= 0) return;
+    const int sq = rows.slab ? (int)(r / rows.J) : seq_of(b.cu_q, b.B, t);
+    const int a = sink_pos0 ? max(0, __ldg(sink_pos0 + sq)) : 0;
+    lo = a;
+    hi = (int)min((int64_t)a + n_sink, (int64_t)0x7fffffff);
+}
 }  // namespace
 
 template <int NT>
@@ -101,7 +112,8 @@ __device__ __forceinline__ void find_bin(ClusterSmem<NT> &sm, const uint32_t *hi
 
 template <int NT, int KPT>
 __device__ __forceinline__ void select_cluster(ClusterSmem<NT> &sm, uint32_t *stage, const float *row, int n,
-                                               int k, int32_t *out, int C, uint32_t crank, bool vec) {
+                                               int k, int32_t *out, int C, uint32_t crank, bool vec, int sink_lo,
+                                               int sink_hi) {
     constexpr int NW = NT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int GT = C * NT;
@@ -131,6 +143,11 @@ __device__ __forceinline__ void select_cluster(ClusterSmem<NT> &sm, uint32_t *st
     } else {
 #pragma unroll
         for (int j = 0; j < KPT; ++j) key[j] = j < cnt ? float_key(__ldcg(row + s0 + j)) : 0u;
+    }
+    if (sink_hi > sink_lo) {                             // forced-in positions rank first
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)
+            if (j < cnt && s0 + j >= sink_lo && s0 + j < sink_hi) key[j] = 0xFFFFFFFFu;
     }
     if (C > 1) cluster_wait();
     else __syncthreads();
@@ -231,7 +248,8 @@ __device__ __forceinline__ void select_cluster(ClusterSmem<NT> &sm, uint32_t *st
 template <int NT, int KPT>
 __global__ void __launch_bounds__(NT) topk_cluster_kernel(const float *__restrict__ scores, int64_t ld, DevBatch b,
                                                           RowMap rows, int k, int32_t *__restrict__ idx,
-                                                          uint32_t *status, int C, int vec, int early) {
+                                                          uint32_t *status, int C, int vec, int early, int n_sink,
+                                                          const int32_t *__restrict__ sink_pos0) {
     __shared__ ClusterSmem<NT> sm;
     extern __shared__ uint32_t stage[];                 // min(k, NT * KPT) selected positions
     tl_start(b.timeline, kTlTopk);
@@ -252,8 +270,10 @@ __global__ void __launch_bounds__(NT) topk_cluster_kernel(const float *__restric
         } else if (pos + 1 <= k) {
             for (int i = g; i < k; i += GT) out[i] = i <= pos ? i : -1;
         } else {
+            int lo, hi;
+            row_sink(b, rows, r, t, n_sink, sink_pos0, lo, hi);
             pdl_wait();                                // the scores come from the preceding kernel
-            select_cluster<NT, KPT>(sm, stage, scores + r * ld, pos + 1, k, out, C, crank, vec != 0);
+            select_cluster<NT, KPT>(sm, stage, scores + r * ld, pos + 1, k, out, C, crank, vec != 0, lo, hi);
         }
     }
     __syncthreads();
@@ -265,7 +285,7 @@ __global__ void __launch_bounds__(NT) topk_cluster_kernel(const float *__restric
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restrict__ scores, int64_t ld,
                                                             DevBatch b, RowMap rows, int k,
                                                             int32_t *__restrict__ idx, uint32_t *status,
-                                                            int cap) {
+                                                            int cap, int n_sink, const int32_t *__restrict__ sink_pos0) {
     __shared__ topk::Shared<kTopkThreads> sm;
     extern __shared__ uint32_t keys[];                   // cap keys
     tl_start(b.timeline, kTlTopk);
@@ -281,8 +301,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
         } else if (pos + 1 <= k) {
             for (int i = tid; i < k; i += kTopkThreads) out[i] = i <= pos ? i : -1;
         } else {
+            int lo, hi;
+            row_sink(b, rows, r, t, n_sink, sink_pos0, lo, hi);
             pdl_wait();
-            topk::select_row<kTopkThreads, -1>(sm, tid, keys, cap, scores + r * ld, pos + 1, k, out, nullptr);
+            topk::select_row<kTopkThreads, -1>(sm, tid, keys, cap, topk::RowSrc{scores + r * ld, lo, hi}, pos + 1, k,
+                                               out, nullptr);
         }
     }
     __syncthreads();
@@ -294,7 +317,8 @@ namespace {
 
 template <int NT, int KPT>
 cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k, int32_t *idx,
-                           uint32_t *status, cudaStream_t stream, bool pdl, int64_t nrows, int C, int vec) {
+                           uint32_t *status, cudaStream_t stream, bool pdl, int64_t nrows, int C, int vec,
+                           int n_sink, const int32_t *sink_pos0) {
     if (nrows * C > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const size_t stage = (size_t)std::min(k, NT * KPT) * 4;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_cluster_kernel<NT, KPT>),
@@ -315,7 +339,8 @@ cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, R
     cfg.attrs = attr;
     cfg.numAttrs = C > 1 ? 2 : 1;
     const int early = nrows * C <= kSMs / 4 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<NT, KPT>, scores, ld, b, rows, k, idx, status, C, vec, early);
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<NT, KPT>, scores, ld, b, rows, k, idx, status, C, vec, early,
+                              n_sink, sink_pos0);
 }
 
 }  // namespace
@@ -323,22 +348,27 @@ cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, R
 // Explicit configuration (threads per CTA, keys per thread, cluster size);
 // nt * kpt * C must cover the longest row.
 cudaError_t launch_topk_cfg(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k, int32_t *idx,
-                            uint32_t *status, cudaStream_t stream, bool pdl, int nt, int kpt, int C) {
+                            uint32_t *status, cudaStream_t stream, bool pdl, int nt, int kpt, int C, int n_sink,
+                            const int32_t *sink_pos0) {
     const int64_t nrows = rows.slab ? (int64_t)b.B * rows.J : (int64_t)b.T;
     if (nrows <= 0) return cudaSuccess;
     if (C < 1 || C > kMaxCluster || (int64_t)nt * kpt * C < b.max_kv) return cudaErrorInvalidValue;
     const int vec = (ld % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0) ? 1 : 0;
     if (nt == 512 && kpt == 16)
-        return launch_cluster<512, 16>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec);
+        return launch_cluster<512, 16>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec, n_sink,
+                                                   sink_pos0);
     if (nt == 512 && kpt == 32)
-        return launch_cluster<512, 32>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec);
+        return launch_cluster<512, 32>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec, n_sink,
+                                                   sink_pos0);
     if (nt == 256 && kpt == 32)
-        return launch_cluster<256, 32>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec);
+        return launch_cluster<256, 32>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec, n_sink,
+                                                   sink_pos0);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k,
-                        int32_t *idx, uint32_t *status, cudaStream_t stream, bool pdl) {
+                        int32_t *idx, uint32_t *status, cudaStream_t stream, bool pdl, int n_sink,
+                        const int32_t *sink_pos0) {
     const int64_t nrows = rows.slab ? (int64_t)b.B * rows.J : (int64_t)b.T;
     if (nrows <= 0) return cudaSuccess;
     if (nrows > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -350,18 +380,18 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
     // 8192-key rows).
     if (n_max <= 8192) {
         if (nrows >= 2 * kSMs)
-            return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 256, 32, 1);
-        return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 16, 1);
+            return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 256, 32, 1, n_sink, sink_pos0);
+        return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 16, 1, n_sink, sink_pos0);
     }
     if (n_max <= (int64_t)kMaxCluster * 512 * 32)
         return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 32,
-                               (int)((n_max + 512 * 32 - 1) / (512 * 32)));
+                               (int)((n_max + 512 * 32 - 1) / (512 * 32)), n_sink, sink_pos0);
     int cap = kSmemCapHybrid;
     const size_t smem = (size_t)cap * 4;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_kernel), 2, (size_t)kSmemCapMax * 4);
     if (e != cudaSuccess) return e;
     return launch_k(topk_kernel, dim3((unsigned)nrows), dim3(kTopkThreads), smem, stream, pdl, scores, ld, b,
-                    rows, k, idx, status, cap);
+                    rows, k, idx, status, cap, n_sink, sink_pos0);
 }
 
 }  // namespace dsa

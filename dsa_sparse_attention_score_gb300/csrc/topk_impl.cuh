@@ -83,13 +83,23 @@ __device__ __forceinline__ void clear_hist(Shared<NT> &sm, int tid, int nb) {
     for (int i = tid; i < nb; i += NT) sm.hist[i] = 0;
 }
 
-__device__ __forceinline__ uint32_t row_key(const float *row, int s) { return float_key(__ldcg(row + s)); }
+// A score row and its forced-in (attention-sink) positions [lo, hi), whose
+// keys become the maximum key so that they rank first and tie by position.
+struct RowSrc {
+    const float *p;
+    int lo, hi;
+    __device__ __forceinline__ bool sink(int s) const { return s >= lo && s < hi; }
+};
+
+__device__ __forceinline__ uint32_t row_key(const RowSrc &row, int s) {
+    return row.sink(s) ? 0xFFFFFFFFu : float_key(__ldcg(row.p + s));
+}
 
 // Histogram of digit (key >> sh) & (nb-1) over the keys whose bits above the
 // digit equal `prefix` (all keys when hsh >= 32), from shared memory or from
 // the float row in global memory.
 template <int NT, bool kShared>
-__device__ __forceinline__ void digit_hist(Shared<NT> &sm, int tid, const uint32_t *keys, const float *row, int n,
+__device__ __forceinline__ void digit_hist(Shared<NT> &sm, int tid, const uint32_t *keys, const RowSrc &row, int n,
                                            int sh, int nb, int hsh, uint32_t prefix) {
     constexpr int U = kShared ? 1 : 8;                   // loads in flight per thread
     for (int s0 = tid; s0 < n; s0 += U * NT) {
@@ -111,7 +121,7 @@ __device__ __forceinline__ void digit_hist(Shared<NT> &sm, int tid, const uint32
 // Ordered compaction over positions 0..n-1: keeps keys > tau and the first
 // need_eq keys == tau, writing positions in ascending order to out.
 template <int NT, int kBar, bool kShared>
-__device__ void compact(Shared<NT> &sm, int tid, const uint32_t *keys, const float *row, int n, uint32_t tau,
+__device__ void compact(Shared<NT> &sm, int tid, const uint32_t *keys, const RowSrc &row, int n, uint32_t tau,
                         uint32_t need_eq, int32_t *out) {
     constexpr int W = NT / 32;
     const int lane = tid & 31, warp = tid >> 5;
@@ -158,7 +168,7 @@ __device__ void compact(Shared<NT> &sm, int tid, const uint32_t *keys, const flo
 // keys: shared scratch for `cap` keys.  first_hist: optional histogram of the
 // top 11 key bits of the row (global memory), which replaces the first pass.
 template <int NT, int kBar>
-__device__ void select_row(Shared<NT> &sm, int tid, uint32_t *keys, int cap, const float *row, int n, int k,
+__device__ void select_row(Shared<NT> &sm, int tid, uint32_t *keys, int cap, const RowSrc &row, int n, int k,
                            int32_t *out, const uint32_t *first_hist) {
     uint32_t prefix = 0, above = 0, kk = (uint32_t)k;
     const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
@@ -169,12 +179,12 @@ __device__ void select_row(Shared<NT> &sm, int tid, uint32_t *keys, int cap, con
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int s = s0 + u * NT;
-                f[u] = s < n ? __ldcg(row + s) : 0.f;
+                f[u] = s < n ? __ldcg(row.p + s) : 0.f;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int s = s0 + u * NT;
-                if (s < n) keys[s] = float_key(f[u]);
+                if (s < n) keys[s] = row.sink(s) ? 0xFFFFFFFFu : float_key(f[u]);
             }
         }
         if (first_hist) {

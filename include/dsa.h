@@ -159,6 +159,24 @@ dsa_status_t dsa_topk(const float *scores, int64_t ld_scores, const dsa_batch_t 
                       int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Top-k with the attention sink forced in ([SINK]: ik_llama_opt commit log,
+ * "GLM-5.2 DSA indexer: per-sequence attention sink" and "UPDATE 6 --
+ * serving-correctness": the first n_sink keys of the query's own sequence,
+ * counted from the sequence's first present position, get a +1e20 boost
+ * before the argsort so they always survive).  Here the boost is unbounded:
+ * for token t of sequence b the positions [a_b, a_b + n_sink) within
+ * [0, q_pos[t]] rank above every score and tie with one another (lower
+ * position first); the rest of the selection is dsa_topk's.
+ *   n_sink     >= 0 (0: exactly dsa_topk)
+ *   sink_pos0  device int32 [B], a_b = max(0, sink_pos0[b]); NULL means a_b = 0
+ * Errors: n_sink < 0 -> DSA_ERR_INVALID_ARGUMENT; sink_pos0 not 4-byte
+ * aligned -> DSA_ERR_MISALIGNED; otherwise as dsa_topk.
+ */
+dsa_status_t dsa_topk_sink(const float *scores, int64_t ld_scores, const dsa_batch_t *batch, int k, int n_sink,
+                           const int32_t *sink_pos0, int32_t *idx, void *ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/*
  * Sparse MLA attention in the absorbed form ([MLA], [ABS]).  For token t and
  * head h, over the selected rows c_j = kv_cache[kv_off[b] + idx[t,j]]:
  *   z_j      = sm_scale * (q_lat[t,h] . c_j[0:512] + q_rope[t,h] . c_j[512:576])
@@ -197,6 +215,17 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
                         const dsa_batch_t *batch, int H_I, int H, int k, float sm_scale,
                         int hadamard, float *out, float *lse, int32_t *idx_out,
                         void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * dsa_decode with the attention sink forced into every token's selection
+ * ([SINK], as dsa_topk_sink: n_sink >= 0, sink_pos0 device int32 [B] or
+ * NULL).  Same workspace, outputs and errors as dsa_decode.
+ */
+dsa_status_t dsa_decode_sink(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                             const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
+                             const dsa_bf16 *kv_cache, const dsa_batch_t *batch, int H_I, int H, int k,
+                             float sm_scale, int hadamard, int n_sink, const int32_t *sink_pos0, float *out,
+                             float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * dsa_decode without a workspace, for callers that cannot allocate device

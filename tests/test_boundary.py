@@ -102,6 +102,12 @@ def test_argument_validation_runs_before_any_launch(L):
                dict(q_pos=0)):
         bb = _batch(**kw)
         assert L.dsa_topk(fake, 100, C.byref(bb), 4, fake, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # attention sink: negative count, misaligned anchors
+    assert L.dsa_topk_sink(fake, 100, C.byref(b), 4, -1, None, fake, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_topk_sink(fake, 100, C.byref(b), 4, 2, C.c_void_p(0x40002), fake, ws, nws, None) == \
+        dsa.DSA_ERR_MISALIGNED
+    assert L.dsa_decode_sink(fake, 0, fake, fake, fake, fake, fake, fake, C.byref(b), 32, 64, 2048, 0.1, 0, -1,
+                             None, fake, None, None, ws, n.value, None) == dsa.DSA_ERR_INVALID_ARGUMENT
     assert L.dsa_set_trace_events(None, -1) == dsa.DSA_ERR_INVALID_ARGUMENT
     assert L.dsa_set_trace_events(None, 0) == dsa.DSA_OK
     assert L.dsa_workspace_init(None, 256, None) == dsa.DSA_ERR_INVALID_ARGUMENT
