@@ -36,7 +36,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "DSA decode tok/s & prefill tok/s on 1 GB300; % of HBM / tensor roofline"
 UNIT = "tok/s"
-WORKLOADS = {"tiny_decode": 1, "batched_decode": 2, "ragged_decode": 3, "prefill_chunk": 4, "long_prefill": 5}
+WORKLOADS = {"tiny_decode": 1, "batched_decode": 2, "ragged_decode": 3, "prefill_chunk": 4, "long_prefill": 5,
+             "indexshare_decode": 2}
+STACK_LAYERS = 78
+
+
+def index_share_full(il: int) -> bool:
+    """ik_llama_opt commit log, "GLM-5.2 DSA: IndexShare (shared layers reuse
+    full-layer top-k)": layer il computes its own top-k iff il <= 1 or
+    il % 4 == 2 (21 of 78 layers); the others reuse the most recent full
+    layer's selection."""
+    return il <= 1 or il % 4 == 2
 STAGES = ["k_append", "indexer_score", "topk", "sparse_attn", "attn_combine"]
 KERNEL_OF_STAGE = {"k_append": "k_append_kernel", "indexer_score": "score_kernel", "topk": "topk_cluster_kernel",
                    "sparse_attn": "sparse_attn_kernel", "attn_combine": "attn_combine_kernel"}
@@ -206,25 +216,206 @@ def reference_arm(args):
         subs.append((one, S.Inputs(k_cache=inp.k_cache[sl], k_new=inp.k_new[t:t + 1], q_idx=inp.q_idx[t:t + 1],
                                    w=inp.w[t:t + 1], q_lat=inp.q_lat[t:t + 1], q_rope=inp.q_rope[t:t + 1],
                                    kv_cache=inp.kv_cache[sl])))
-    for i in range(args.warmup):
+    stack = args.workload == "indexshare_decode"
+
+    def one_step(i):
         one, si = subs[i % len(subs)]
-        oracle.decode(si, one)
+        if not stack:
+            oracle.decode(si, one)
+            return
+        # one token through the layer stack: full layers decode, shared
+        # layers attend over the last full layer's selection
+        idx = None
+        for il in range(STACK_LAYERS):
+            if index_share_full(il):
+                idx = oracle.decode(si, one)["idx"]
+            else:
+                oracle.sparse_attn(si.q_lat, si.q_rope, si.kv_cache, oracle.Batch.of(one), idx, one.sm_scale)
+
+    for i in range(args.warmup):
+        one_step(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        one, si = subs[i % len(subs)]
-        oracle.decode(si, one)
+        one_step(i)
     el = time.perf_counter() - t0
     value = args.steps / el
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H_I": wl.H_I, "H": wl.H, "top_k": wl.top_k,
-                       "step": "one query token of the workload (its sequence's full key range)"},
+            "config": {"workload": (f"indexshare_decode_B8_L8192_{STACK_LAYERS}layers" if stack else wl.name),
+                       "B": wl.B, "T": wl.T, "H_I": wl.H_I, "H": wl.H, "top_k": wl.top_k,
+                       "step": "one query token of the workload (its sequence's full key range)"
+                               + (f" through {STACK_LAYERS} layers" if stack else "")},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} steps, one query token each, cycling over the "
                                        f"{len(subs)} first tokens of {wl.name}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- layer stack (IndexShare)
+
+def layer_stack(args):
+    """Decode through a stack of STACK_LAYERS layers of the batched-decode
+    shapes.  Full layers run dsa_decode (append, score, top-k, attention) and
+    keep their selection; shared layers run dsa_sparse_mla_attn on the most
+    recent full layer's selection.  The same stack with every layer full is
+    timed beside it.  Each layer has its own caches (about 92 MB), generated
+    on the device from a seeded generator with the shapes and scales of the
+    single-layer inputs, so no layer finds another's rows in L2."""
+    import torch
+    torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    from dsa_sparse_attention_score_gb300 import build as lib_build
+    lib_build.build()
+    import dsa_sparse_attention_score_gb300 as dsa
+    import dsa_synth as S
+    wl = S.config(2)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(20260)
+
+    def normal(shape, scale, dtype):
+        return (torch.randn(shape, generator=g, device="cuda", dtype=torch.float32) * scale).to(dtype)
+
+    rows, T = wl.cache_rows, wl.T
+    # per-step inputs of every layer packed in one buffer (256-B aligned
+    # slots), so the end-to-end loop moves them with one copy
+    step_shapes = [("k_new", (T, 128), torch.float32, 128 ** -0.5), ("q_idx", (T, wl.H_I, 128), torch.float16, 128 ** -0.5),
+                   ("w", (T, wl.H_I), torch.float32, wl.H_I ** -0.5), ("q_lat", (T, wl.H, 512), torch.bfloat16, 512 ** -0.5),
+                   ("q_rope", (T, wl.H, 64), torch.bfloat16, 64 ** -0.5)]
+    slot = []
+    total = 0
+    for name, shp, dt, _ in step_shapes:
+        nb = math.prod(shp) * torch.empty((), dtype=dt).element_size()
+        slot.append((total, nb))
+        total += (nb + 255) // 256 * 256
+    d_pack = torch.empty(STACK_LAYERS * total, dtype=torch.uint8, device="cuda")
+    layers = []
+    for il in range(STACK_LAYERS):
+        L = dict(k_cache=normal((rows, 128), 128 ** -0.5, torch.float16),
+                 kv_cache=normal((rows, 576), 576 ** -0.5, torch.bfloat16))
+        for (name, shp, dt, sc), (off, nb) in zip(step_shapes, slot):
+            v = d_pack[il * total + off: il * total + off + nb].view(dt).view(shp)
+            v.copy_(normal(shp, sc, dt))
+            L[name] = v
+        layers.append(L)
+    h_pack = d_pack.cpu().pin_memory()
+    batch = dsa.Batch.from_host(wl.cu_q, wl.q_pos, wl.kv_off, wl.cache_rows, max_q_per_seq=1, max_kv=wl.max_kv)
+    ws = dsa.workspace(dsa.DSA_OP_DECODE, batch, wl.H_I, wl.H, wl.top_k)
+    out = torch.empty((T, wl.H, 512), device="cuda")
+    lse = torch.empty((T, wl.H), device="cuda")
+    idx = torch.empty((T, wl.top_k), dtype=torch.int32, device="cuda")
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones((args.flush_mb << 20) // 4, dtype=torch.float32, device="cuda")
+
+    def step(share):
+        for il, L in enumerate(layers):
+            if not share or index_share_full(il):
+                dsa.dsa_decode(L["k_new"], L["q_idx"], L["w"], L["q_lat"], L["q_rope"], L["k_cache"],
+                               L["kv_cache"], batch, wl.top_k, wl.sm_scale, wl.hadamard, out, lse, idx, ws)
+            else:
+                dsa.dsa_sparse_mla_attn(L["q_lat"], L["q_rope"], L["kv_cache"], batch, idx, wl.sm_scale, out,
+                                        lse, ws)
+
+    res = {}
+    for share in (True, False):
+        step(share)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(share)
+        for i in range(args.warmup):
+            flush.fill_(i & 0xFF)
+            flush_r.amax()
+            graph.replay()
+        torch.cuda.synchronize()
+        clocks = Clocks(gpu_index_for(dev))
+        time.sleep(0.2)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            flush_r.amax()
+            ev[i][0].record()
+            graph.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        rows_c = clocks.stop()
+        ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+        res[share] = (ms, Clocks.summary(rows_c))
+        if dsa.dsa_read_device_status(ws) != 0:
+            raise RuntimeError("device status flags set during the timed steps")
+    # end to end through the public API: one pinned H2D copy of every layer's
+    # step inputs, the IndexShare stack, a D2H read of the last layer's output
+    graph = torch.cuda.CUDAGraph()
+    step(True)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        step(True)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for i in range(min(args.steps, args.e2e_steps) + 3):
+        flush.fill_(i & 0xFF)
+        flush_r.amax()
+        e0.record()
+        d_pack.copy_(h_pack, non_blocking=True)
+        step(True)
+        h_out.copy_(out, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_step = statistics.fmean(e2e_ms)
+    n_full = sum(index_share_full(il) for il in range(STACK_LAYERS))
+    per_full = dsa.dsa_decode_launches(batch, wl.H_I, wl.H, wl.top_k)
+    per_shared = per_full - 2                        # attention (+ combine) only
+    alg = algorithmic(wl)
+    step_bytes = n_full * alg["step_bytes"] + (STACK_LAYERS - n_full) * alg["attn_bytes"]
+    ms, clk = res[True]
+    pk = peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16+bf16 (f32 accumulate)",
+        "data": "synthetic (device generator, seeded)",
+        "config": {"workload": f"indexshare_decode_B8_L8192_{STACK_LAYERS}layers", "B": wl.B, "T": T,
+                   "L": wl.max_kv, "H_I": wl.H_I, "H": wl.H, "top_k": wl.top_k, "layers": STACK_LAYERS,
+                   "full_layers": n_full, "shared_layers": STACK_LAYERS - n_full,
+                   "l2": f"flushed before every timed step ({args.flush_mb} MB write, then read)",
+                   "launch": "CUDA graph replay of the whole stack", "parallelism": "replicas x1"},
+        "clocks": clk,
+        "gpu_launches": (n_full * per_full + (STACK_LAYERS - n_full) * per_shared) * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "algorithmic_bytes_per_step": step_bytes,
+                     "kernel": "whole stack", "traffic": None},
+        "all_full_layers": {"ms_per_step": res[False][0], "tok_s": T / (res[False][0] * 1e-3),
+                            "clocks": res[False][1]},
+        "index_share_speedup": res[False][0] / ms,
+        "e2e": {"value": T / (e2e_step * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h_pack.numel(),
+                "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": len(e2e_ms),
+                "path": "one pinned H2D copy of every layer's step inputs, the stack through the Python "
+                        "binding (eager launches), D2H of the last layer's output"},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        cores = oracle.set_threads(0)
+        one = S.Workload(wl.name, wl.seed, [wl.q_pos[0] + 1], [wl.q_pos[0]], [0, 1], wl.H_I, wl.H, wl.top_k,
+                         wl.hadamard, wl.sm_scale)
+        si = S.make_inputs(one)
+        t0 = time.perf_counter()
+        idx1 = None
+        for il in range(STACK_LAYERS):
+            if index_share_full(il):
+                idx1 = oracle.decode(si, one)["idx"]
+            else:
+                oracle.sparse_attn(si.q_lat, si.q_rope, si.kv_cache, oracle.Batch.of(one), idx1, one.sm_scale)
+        el = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 1.0 / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"one query token (L=8192) through the {STACK_LAYERS}-layer IndexShare "
+                                          f"stack, {el:.1f} s on {cores} OpenMP threads"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -235,6 +426,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.workload == "indexshare_decode":
+        return layer_stack(args)
 
     import numpy as np
     import torch
