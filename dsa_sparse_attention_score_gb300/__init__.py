@@ -63,6 +63,8 @@ SIGNATURES = {
     "dsa_decode": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _P, _P, _P, _P, _SZ, _P]),
     "dsa_decode_sink": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _P,
                              _SZ, _P]),
+    "dsa_decode_paged": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, C.c_void_p, _I, _I, _I, _F, _I, _P, _P, _P, _P,
+                              _SZ, _P]),
     "dsa_decode_noalloc": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "dsa_workspace_size": (_I, [_I, _BP, _I, _I, _I, C.POINTER(C.c_size_t)]),
     "dsa_workspace_init": (_I, [_P, _SZ, _P]),
@@ -272,6 +274,37 @@ def dsa_decode(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch: Batch, 
                             _ptr(kv_cache), C.byref(d), q_idx.shape[1], q_lat.shape[1], k, sm_scale,
                             int(hadamard), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws), ws.numel(),
                             _stream(stream)), "dsa_decode")
+
+
+class dsa_paging_t(C.Structure):
+    _fields_ = [("block_table", C.c_void_p), ("max_blocks", C.c_int32), ("block_size", C.c_int32)]
+
+
+def dsa_decode_paged(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch: Batch, block_table,
+                     block_size: int, k: int, sm_scale: float, hadamard: bool, out, lse, idx_out, ws,
+                     stream=None):
+    """dsa_decode over paged caches: block_table is an int32 CUDA tensor
+    [B, max_blocks]; position pos of sequence b lives at cache row
+    block_table[b, pos // block_size] * block_size + pos % block_size."""
+    import torch
+    kd = DSA_KEY_F16 if k_new.dtype == torch.float16 else DSA_KEY_F32
+    _req(k_new, torch.float16 if kd == DSA_KEY_F16 else torch.float32, "k_new")
+    _req(q_idx, torch.float16, "q_idx")
+    _req(w, torch.float32, "w")
+    _req(q_lat, torch.bfloat16, "q_lat")
+    _req(q_rope, torch.bfloat16, "q_rope")
+    _req(k_cache, torch.float16, "k_cache")
+    _req(kv_cache, torch.bfloat16, "kv_cache")
+    _req(block_table, torch.int32, "block_table")
+    _req(out, torch.float32, "out")
+    _req(lse, torch.float32, "lse")
+    _req(idx_out, torch.int32, "idx_out")
+    d = batch.desc()
+    pg = dsa_paging_t(block_table.data_ptr(), block_table.shape[1], block_size)
+    _check(lib().dsa_decode_paged(_ptr(k_new), kd, _ptr(q_idx), _ptr(w), _ptr(q_lat), _ptr(q_rope), _ptr(k_cache),
+                                  _ptr(kv_cache), C.byref(d), C.byref(pg), q_idx.shape[1], q_lat.shape[1], k,
+                                  sm_scale, int(hadamard), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "dsa_decode_paged")
 
 
 def dsa_decode_sink(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch: Batch, k: int, sm_scale: float,

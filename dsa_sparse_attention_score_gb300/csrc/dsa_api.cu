@@ -23,13 +23,13 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-dsa_status_t check_batch(const dsa_batch_t *b) {
+dsa_status_t check_batch(const dsa_batch_t *b, bool paged = false) {
     if (!b) return DSA_ERR_INVALID_ARGUMENT;
     if (b->batch < 1 || b->total_q < 1 || b->max_q_per_seq < 1 || b->max_kv < 1 || b->cache_rows < 1)
         return DSA_ERR_INVALID_ARGUMENT;
     if (b->cache_rows > INT32_MAX || (int64_t)b->batch * b->max_q_per_seq < b->total_q)
         return DSA_ERR_INVALID_ARGUMENT;
-    if (!b->cu_q || !b->q_pos || !b->kv_off) return DSA_ERR_INVALID_ARGUMENT;
+    if (!b->cu_q || !b->q_pos || (!b->kv_off && !paged)) return DSA_ERR_INVALID_ARGUMENT;
     return DSA_OK;
 }
 
@@ -44,6 +44,9 @@ DevBatch dev_batch(const dsa_batch_t *b) {
     d.q_pos = b->q_pos;
     d.kv_off = b->kv_off;
     d.timeline = g_timeline;
+    d.block_table = nullptr;
+    d.max_blocks = 0;
+    d.block_size = 0;
     return d;
 }
 
@@ -164,8 +167,13 @@ inline void trace(int i, cudaStream_t s) {
 dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const dsa_bf16 *kv_cache,
                            const dsa_batch_t *batch, const int32_t *idx, int k, int H, float sm_scale,
                            float *out, float *lse, void *ws, const Layout &L, cudaStream_t stream,
-                           bool traced, bool pdl) {
-    const DevBatch db = dev_batch(batch);
+                           bool traced, bool pdl, const dsa_paging_t *paging = nullptr) {
+    DevBatch db = dev_batch(batch);
+    if (paging) {
+        db.block_table = paging->block_table;
+        db.max_blocks = paging->max_blocks;
+        db.block_size = paging->block_size;
+    }
     CUtensorMap ql, qr, kv;
     const uint64_t qrows = (uint64_t)batch->total_q * H;
     if (!make_map(&ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_lat, D_L, qrows, 64, 64) ||
@@ -371,9 +379,16 @@ static dsa_status_t decode_impl(const void *k_new, int k_dtype, const dsa_f16 *q
                                 const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
                                 const dsa_bf16 *kv_cache, const dsa_batch_t *batch, int H_I, int H, int k,
                                 float sm_scale, int hadamard, int n_sink, const int32_t *sink_pos0, float *out,
-                                float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    dsa_status_t s = check_batch(batch);
+                                float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream,
+                                const dsa_paging_t *paging = nullptr) {
+    dsa_status_t s = check_batch(batch, paging != nullptr);
     if (s != DSA_OK) return s;
+    if (paging) {
+        if (!paging->block_table || paging->block_size < 64 || paging->block_size % 64 != 0 ||
+            (int64_t)paging->max_blocks * paging->block_size < batch->max_kv)
+            return DSA_ERR_INVALID_ARGUMENT;
+        if (!aligned(paging->block_table, 4)) return DSA_ERR_MISALIGNED;
+    }
     if (n_sink < 0) return DSA_ERR_INVALID_ARGUMENT;
     if (sink_pos0 && !aligned(sink_pos0, 4)) return DSA_ERR_MISALIGNED;
     if (!k_new || !q_idx || !w || !q_lat || !q_rope || !k_cache || !kv_cache || !out)
@@ -388,13 +403,21 @@ static dsa_status_t decode_impl(const void *k_new, int k_dtype, const dsa_f16 *q
     const Layout L = layout(DSA_OP_DECODE, batch, k);
     if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
 
-    const DevBatch db = dev_batch(batch);
+    DevBatch db = dev_batch(batch);
+    if (paging) {
+        db.block_table = paging->block_table;
+        db.max_blocks = paging->max_blocks;
+        db.block_size = paging->block_size;
+    }
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     uint32_t *st = status_ptr(ws);
     float *slab = reinterpret_cast<float *>(w8 + L.scores);
     int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(w8 + L.idx);
     CUtensorMap km;
-    if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_cache, D_I, (uint64_t)batch->cache_rows, 64, 128))
+    // paged caches with blocks that are not a multiple of a 128-key tile
+    // load each tile as two 64-row halves
+    const uint32_t key_box_rows = (paging && paging->block_size % 128 != 0) ? 64 : 128;
+    if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_cache, D_I, (uint64_t)batch->cache_rows, 64, key_box_rows))
         return DSA_ERR_CUDA;
 
     // Decode batches (one query token per sequence) append inside the score
@@ -427,7 +450,8 @@ static dsa_status_t decode_impl(const void *k_new, int k_dtype, const dsa_f16 *q
         DSA_TRY_CUDA(launch_topk(slab, L.ld, db, a.rows, k, idx, st, stream, true, n_sink, sink_pos0));
     }
     trace(3, stream);
-    s = run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream, true, true);
+    s = run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream, true, true,
+                      paging);
     if (L.n_split <= 1) trace(4, stream);
     trace(5, stream);
     return s;
@@ -440,6 +464,16 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
                         size_t ws_bytes, cudaStream_t stream) {
     return decode_impl(k_new, k_dtype, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch, H_I, H, k, sm_scale,
                        hadamard, 0, nullptr, out, lse, idx_out, ws, ws_bytes, stream);
+}
+
+dsa_status_t dsa_decode_paged(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                              const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
+                              const dsa_bf16 *kv_cache, const dsa_batch_t *batch, const dsa_paging_t *paging,
+                              int H_I, int H, int k, float sm_scale, int hadamard, float *out, float *lse,
+                              int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!paging) return DSA_ERR_INVALID_ARGUMENT;
+    return decode_impl(k_new, k_dtype, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch, H_I, H, k, sm_scale,
+                       hadamard, 0, nullptr, out, lse, idx_out, ws, ws_bytes, stream, paging);
 }
 
 dsa_status_t dsa_decode_sink(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,

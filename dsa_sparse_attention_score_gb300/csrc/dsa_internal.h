@@ -39,9 +39,25 @@ struct DevBatch {
     int64_t cache_rows;
     const int32_t *cu_q;
     const int32_t *q_pos;
-    const int64_t *kv_off;
+    const int64_t *kv_off;          // null with a block table
     unsigned long long *timeline;   // optional [2 * kTimelineSlots] start/end ns (tracing)
+    // Paged caches: position pos of sequence seq lives at cache row
+    // block_table[seq * max_blocks + pos / block_size] * block_size + pos % block_size.
+    const int32_t *block_table;     // null: contiguous, row kv_off[seq] + pos
+    int max_blocks, block_size;
 };
+
+// Cache row of position pos (0 <= pos < max_kv) of sequence seq, whose
+// contiguous base is kv0 (unused with a block table); -1 for an unmapped
+// block.
+__device__ __forceinline__ int64_t cache_row(const DevBatch &b, int seq, int64_t kv0, int pos) {
+    if (!b.block_table) return kv0 + pos;
+    const int blk = __ldg(b.block_table + (int64_t)seq * b.max_blocks + pos / b.block_size);
+    return blk < 0 ? -1 : (int64_t)blk * b.block_size + pos % b.block_size;
+}
+__device__ __forceinline__ int64_t seq_base(const DevBatch &b, int seq) {
+    return b.kv_off ? __ldg(b.kv_off + seq) : 0;
+}
 
 // Tracing slots of the kernels (earliest CTA start, latest CTA end).
 enum { kTlAppend = 0, kTlScore = 1, kTlTopk = 2, kTlAttn = 3, kTlCombine = 4, kTimelineSlots = 5 };

@@ -38,8 +38,9 @@ __global__ void __launch_bounds__(128) k_append_kernel(const void *__restrict__ 
         v[3] = __half2float(__ushort_as_half((unsigned short)(x.y >> 16)));
     }
     const int s = seq_of_warp(b.cu_q, b.B, t, lane);
-    const int64_t row = __ldg(b.kv_off + s) + pos;
-    if (pos < 0 || pos >= b.max_kv || row < 0 || row >= b.cache_rows) {
+    const int64_t kv0 = seq_base(b, s);
+    const int64_t row = (pos >= 0 && pos < b.max_kv && kv0 >= 0) ? cache_row(b, s, kv0, pos) : -1;
+    if (row < 0 || row >= b.cache_rows) {
         if (lane == 0) flag(status, DSA_DEV_BAD_POSITION);
         return;
     }

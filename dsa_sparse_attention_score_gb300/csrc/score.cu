@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     if (threadIdx.x == 0) {                       // three independent loads
         sm.meta_q0 = __ldg(b.cu_q + seq);
         sm.meta_q1 = __ldg(b.cu_q + seq + 1);
-        sm.meta_kv0 = __ldg(b.kv_off + seq);
+        sm.meta_kv0 = seq_base(b, seq);
     }
     __syncthreads();
     const int q0 = sm.meta_q0, q1 = sm.meta_q1;
@@ -240,7 +240,11 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         const int i = threadIdx.x;
         const int t = q0 + j_lo + i;
         const int pos = __ldg(b.q_pos + t);
-        const bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0 && kv0 + pos < b.cache_rows;
+        bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0;
+        if (ok) {
+            const int64_t row = cache_row(b, seq, kv0, pos);
+            ok = row >= 0 && row < b.cache_rows;
+        }
         if (!ok) flag(p.status, DSA_DEV_BAD_POSITION);
         sm.pos[i] = ok ? pos : -1;
         sm.out_row[i] = p.rows.slab ? (int64_t)seq * p.rows.J + (j_lo + i - p.rows.j0) : (int64_t)t;
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         if (append_tile >= 0) {
             const int t = q0 + j_lo;
             const uint2 kv = appended_key(p.k_new, p.k_dtype, t, p.hadamard_k, lane);
-            reinterpret_cast<uint2 *>(p.k_cache + (kv0 + max_p) * D_I)[lane] = kv;   // persist
+            reinterpret_cast<uint2 *>(p.k_cache + cache_row(b, seq, kv0, max_p) * D_I)[lane] = kv;   // persist
             reinterpret_cast<uint2 *>(sm.new_key)[lane] = kv;                        // staging
         }
     }
@@ -309,10 +313,26 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
                 if (!wait_bar(smem_u32(&sm.empty[s]), (k & 1) ^ 1, sm, p.status)) break;
                 const uint32_t full = smem_u32(&sm.full[s]);
                 mbar_arrive_expect_tx(full, kTileBytes);
-                const int32_t row = (int32_t)(kv0 + chunk0 + (int64_t)i * kTileKeys);
                 const uint32_t dst = smem_u32(stages + s * kTileBytes);
-                tma_load_2d(dst, &k_map, full, 0, row);
-                tma_load_2d(dst + kTileBytes / 2, &k_map, full, 64, row);
+                const int p0 = (int)(chunk0 + (int64_t)i * kTileKeys);
+                if (!b.block_table) {
+                    const int32_t row = (int32_t)(kv0 + p0);
+                    tma_load_2d(dst, &k_map, full, 0, row);
+                    tma_load_2d(dst + kTileBytes / 2, &k_map, full, 64, row);
+                } else {
+                    // paged: a 128-key tile is one block span when the block
+                    // size is a multiple of 128, else two 64-row halves (the
+                    // map's box is then 64 rows).  Positions past the
+                    // sequence's blocks load the fill value (row cache_rows).
+                    const int halves = b.block_size % kTileKeys == 0 ? 1 : 2;
+                    for (int h = 0; h < halves; ++h) {
+                        const int ph = p0 + h * 64;
+                        int64_t r = ph < b.max_kv ? cache_row(b, seq, kv0, ph) : -1;
+                        if (r < 0 || r >= b.cache_rows) r = b.cache_rows;
+                        tma_load_2d(dst + h * 8192, &k_map, full, 0, (int32_t)r);
+                        tma_load_2d(dst + kTileBytes / 2 + h * 8192, &k_map, full, 64, (int32_t)r);
+                    }
+                }
             }
         }
     } else if (warp == 1) {

@@ -142,10 +142,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tl_start(b.timeline, kTlAttn);
     const int pos = __ldg(b.q_pos + t);
     const int seq = seq_of_warp(b.cu_q, b.B, t, lane);
-    const int64_t kv0 = __ldg(b.kv_off + seq);
+    const int64_t kv0 = seq_base(b, seq);
     const int tile_lo = split * p.tiles_per_cta;
     const int tile_hi = min(p.n_tiles, tile_lo + p.tiles_per_cta);
-    const bool pos_ok = pos >= 0 && pos < b.max_kv && kv0 >= 0 && kv0 + pos < b.cache_rows;
+    int64_t own_row = -1;                                // the token's own row: fallback for skipped entries
+    if (pos >= 0 && pos < b.max_kv && kv0 >= 0) own_row = cache_row(b, seq, kv0, pos);
+    const bool pos_ok = own_row >= 0 && own_row < b.cache_rows;
     if (!pos_ok || tile_lo >= tile_hi) {
         if (!pos_ok && threadIdx.x == 0 && split == 0) flag(p.status, DSA_DEV_BAD_POSITION);
         // Empty contribution.
@@ -219,9 +221,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 4; ++j) {
                     const int e = (tile_lo + it) * kRows + quad * 4 + j;
                     const int32_t v = e < p.k ? __ldg(idx_row + e) : -1;
-                    const bool ok = v >= 0 && v <= pos;
+                    bool ok = v >= 0 && v <= pos;
+                    int64_t row;
+                    if (!b.block_table) {
+                        row = kv0 + (ok ? v : pos);      // in range: the position check covers v <= pos
+                    } else {
+                        row = ok ? cache_row(b, seq, kv0, v) : own_row;
+                        if (row < 0 || row >= b.cache_rows) {
+                            ok = false;
+                            row = own_row;
+                        }
+                    }
                     if (!ok && v != -1 && kb == 0) flag(p.status, DSA_DEV_BAD_INDEX);
-                    rr[j] = (int32_t)(kv0 + (ok ? v : 0));
+                    rr[j] = (int32_t)row;
                 }
                 tma_gather4(smem_u32(c_s + buf * kCBytes + kb * kCBlockBytes + quad * 512), &kv_map, full, kb * 64,
                             rr[0], rr[1], rr[2], rr[3]);

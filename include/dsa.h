@@ -217,6 +217,41 @@ dsa_status_t dsa_decode(const void *k_new, int k_dtype, const dsa_f16 *q_idx, co
                         void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Paged caches ([PAGE]: vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on
+ * gfx1030": the latent cache and the indexer cache are two paged attention
+ * groups of the serving engine, and the DSA backend gathers the selected
+ * latents through the page table).  Position pos of sequence b is cache row
+ *   block_table[b * max_blocks + pos / block_size] * block_size + pos % block_size
+ * of both k_cache and kv_cache.
+ *   block_table  device int32 [B, max_blocks]; entries of blocks a sequence
+ *                does not reach are never read past max_kv; a negative
+ *                entry marks an unmapped block (positions there are
+ *                flagged DSA_DEV_BAD_POSITION / DSA_DEV_BAD_INDEX)
+ *   block_size   a multiple of 64 (tiles load as 64-row halves unless it is
+ *                a multiple of 128)
+ *   max_blocks   >= ceil(max_kv / block_size)
+ */
+typedef struct {
+    const int32_t *block_table;
+    int32_t max_blocks;
+    int32_t block_size;
+} dsa_paging_t;
+
+/*
+ * dsa_decode over paged caches (see dsa_paging_t).  batch->kv_off is not
+ * read (it may be NULL); batch->cache_rows is the row count of both pooled
+ * caches.  Errors as dsa_decode, plus DSA_ERR_INVALID_ARGUMENT for a null
+ * paging, a null block table, a block size that is not a positive multiple
+ * of 64, or max_blocks * block_size < max_kv, and DSA_ERR_MISALIGNED for a
+ * block table that is not 4-byte aligned.
+ */
+dsa_status_t dsa_decode_paged(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
+                              const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, dsa_f16 *k_cache,
+                              const dsa_bf16 *kv_cache, const dsa_batch_t *batch, const dsa_paging_t *paging,
+                              int H_I, int H, int k, float sm_scale, int hadamard, float *out, float *lse,
+                              int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * dsa_decode with the attention sink forced into every token's selection
  * ([SINK], as dsa_topk_sink: n_sink >= 0, sink_pos0 device int32 [B] or
  * NULL).  Same workspace, outputs and errors as dsa_decode.
