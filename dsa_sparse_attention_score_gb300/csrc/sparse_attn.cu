@@ -208,15 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem_u32(q_s + 8 * kQBlockBytes), &q_rope_map, qf, 0, qrow);
         }
         pdl_wait();                                  // the indices come from the preceding kernel
+        // Rows of this thread's requests (at most two: 144 per tile, 128
+        // producers) are looked up before the buffer is free, so the copies
+        // go out as soon as it is.
+        constexpr int kReq = ((kRows / 4) * kBlocks + kProducers - 1) / kProducers;
         for (int it = 0; it < n_my; ++it) {
             const int buf = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
-            if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status)) break;
-            const uint32_t full = smem_u32(&ctl.c_full[buf]);
-            if (pl == 0) mbar_arrive_expect_tx(full, kCBytes);
-            for (int q = pl; q < (kRows / 4) * kBlocks; q += kProducers) {
+            int32_t rr[kReq][4];
+#pragma unroll
+            for (int u = 0; u < kReq; ++u) {
+                const int q = pl + u * kProducers;
+                if (q >= (kRows / 4) * kBlocks) break;
                 const int quad = q / kBlocks, kb = q % kBlocks;
-                int32_t rr[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int e = (tile_lo + it) * kRows + quad * 4 + j;
@@ -233,10 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (!ok && v != -1 && kb == 0) flag(p.status, DSA_DEV_BAD_INDEX);
-                    rr[j] = (int32_t)row;
+                    rr[u][j] = (int32_t)row;
                 }
+            }
+            if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status)) break;
+            const uint32_t full = smem_u32(&ctl.c_full[buf]);
+            if (pl == 0) mbar_arrive_expect_tx(full, kCBytes);
+#pragma unroll
+            for (int u = 0; u < kReq; ++u) {
+                const int q = pl + u * kProducers;
+                if (q >= (kRows / 4) * kBlocks) break;
+                const int quad = q / kBlocks, kb = q % kBlocks;
                 tma_gather4(smem_u32(c_s + buf * kCBytes + kb * kCBlockBytes + quad * 512), &kv_map, full, kb * 64,
-                            rr[0], rr[1], rr[2], rr[3]);
+                            rr[u][0], rr[u][1], rr[u][2], rr[u][3]);
             }
         }
     } else if (warp == kMmaWarp) {
