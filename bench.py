@@ -168,6 +168,25 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest value of x over the ranks of the job (the job takes as
+    long as its slowest replica); x itself outside a multi-rank job."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, seconds: float) -> float:
+    """Whole-job tokens per second: every rank runs its own replica of the
+    workload (weak scaling), so the job processes world x tokens per step."""
+    return world * tokens_per_step * steps / seconds
+
+
 def gpu_index_for(device):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -585,13 +604,9 @@ def main():
         torch.distributed.barrier()
     clock_rows = clocks.stop()
 
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        tt = torch.tensor([total_s], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(tt.item())
+    total_s = max_over_ranks(sum(step_ms) / 1e3)
     ms_per_step = 1e3 * total_s / args.steps
-    value = world * wl.T * args.steps / total_s
+    value = job_throughput(world, wl.T, args.steps, total_s)
 
     # ---- end to end through the public API with host buffers
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -610,12 +625,8 @@ def main():
         e1.synchronize()
         if i >= 3:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_s = sum(e2e_ms) / 1e3
-    if world > 1:
-        tt = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    e2e_value = world * wl.T * n_e2e / e2e_s
+    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3)
+    e2e_value = job_throughput(world, wl.T, n_e2e, e2e_s)
     if dsa.dsa_read_device_status(ws) != 0:
         raise RuntimeError("device status flags set during the timed steps")
 
