@@ -525,12 +525,15 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     const int64_t span = a.fill_masked ? a.ld : (int64_t)b.max_kv;
     const int64_t tiles = (span + kTileKeys - 1) / kTileKeys;
     const int64_t work = tiles * (int64_t)b.B * p.groups_per_seq;
-    // About two CTAs' worth of tiles per SM; short chunks (small decode
-    // batches) run with a 2-deep ring so that several CTAs share an SM.
+    // About two CTAs' worth of tiles per SM.
     int64_t tpc = (work + 2 * 152 - 1) / (2 * 152);
     tpc = std::max<int64_t>(2, std::min<int64_t>(64, tpc));
     p.tiles_per_cta = (int)tpc;
-    p.stages = tpc <= 2 ? 2 : kMaxStages;
+    // One-token groups (decode variant, launched two CTAs per SM) use a
+    // 2-deep ring so that two CTAs fit: measured on GB300 on the ragged
+    // long-context decode, 90 us against 128 us with a 4-deep ring at one CTA
+    // per SM.
+    p.stages = (p.G == 1 || tpc <= 2) ? 2 : kMaxStages;
     const int64_t chunks = (tiles + tpc - 1) / tpc;
     const int64_t groups = (int64_t)b.B * p.groups_per_seq;
     if (groups > 65535 || chunks > 0x7fffffff) return cudaErrorInvalidConfiguration;
