@@ -426,7 +426,7 @@ static dsa_status_t decode_impl(const void *k_new, int k_dtype, const dsa_f16 *q
     trace(0, stream);
     if (!fuse_append)
         DSA_TRY_CUDA(launch_k_append(k_new, k_dtype, db, k_cache, hadamard != 0, st, stream));
-    for (int j0 = 0; j0 < batch->max_q_per_seq; j0 += L.J) {
+    for (int j0 = 0, win = 0; j0 < batch->max_q_per_seq; j0 += L.J, ++win) {
         ScoreLaunch a{};
         a.q_idx = q_idx;
         a.w = w;
@@ -447,7 +447,9 @@ static dsa_status_t decode_impl(const void *k_new, int k_dtype, const dsa_f16 *q
         if (j0 == 0) trace(1, stream);
         DSA_TRY_CUDA(launch_score(a, km, db, st, stream, !(fuse_append && j0 == 0)));
         if (j0 == 0) trace(2, stream);
+        trace(6 + 2 * win, stream);
         DSA_TRY_CUDA(launch_topk(slab, L.ld, db, a.rows, k, idx, st, stream, true, n_sink, sink_pos0));
+        trace(7 + 2 * win, stream);
     }
     trace(3, stream);
     s = run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream, true, true,

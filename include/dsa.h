@@ -326,7 +326,11 @@ const char *dsa_status_string(dsa_status_t status);
  * Profiling hook (not thread-safe).  When set, dsa_decode records
  * events[0..n) on its stream at stage boundaries: before the append, the
  * first score launch, the first top-k launch, the attention and the combine,
- * and after the last launch (6 events).  n = 0 or events = NULL disables it.
+ * and after the last launch (6 events).  Calls that score in several
+ * windows of query tokens also record events[6 + 2j] and events[7 + 2j]
+ * just before and after the top-k launch of window j (when j < (n - 6) / 2).
+ * Slots left unrecorded keep their previous timestamp.  n = 0 or
+ * events = NULL disables it.
  */
 dsa_status_t dsa_set_trace_events(cudaEvent_t *events, int n);
 
