@@ -29,6 +29,7 @@ DSA_ERR_DEVICE = 6
 DSA_DEV_BAD_POSITION = 1
 DSA_DEV_BAD_INDEX = 2
 DSA_DEV_TIMEOUT = 4
+DSA_DEV_SMEM_LAYOUT = 8
 
 DSA_KEY_F32 = 0
 DSA_KEY_F16 = 1

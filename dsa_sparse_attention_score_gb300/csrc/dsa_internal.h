@@ -133,6 +133,6 @@ int attn_tile_rows();
 
 // Shared-memory bytes of the attention kernel (for the host's occupancy set-up).
 size_t sparse_attn_smem_bytes();
-size_t score_smem_bytes(int n_pad, int hadamard_q, int n_stages);
+size_t score_smem_bytes(int n_rows, int hadamard_q, int n_stages);
 
 }  // namespace dsa

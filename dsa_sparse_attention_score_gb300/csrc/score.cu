@@ -9,11 +9,14 @@
 // One CTA owns a group of up to G query tokens of one sequence and a chunk of
 // consecutive 128-key tiles.  Per tile the tensor core computes
 //     D[key, (token, head)] = k_tile[128 x 128] . Q[(token, head) x 128]^T
-// (M = 128 keys, N = G * HP with HP = H_I rounded up to 16, K = 128) into a
-// double-buffered TMEM accumulator, so the epilogue of tile i overlaps the
-// MMA of tile i+1 and the TMA loads of tiles i+2.. .  In the epilogue each
-// thread owns one key row (its TMEM lane) and reduces sum_h w * max(0, D) for
-// each of its tokens in registers -- no cross-thread reduction.
+// (M = 128 keys, K = 128, HP = H_I rounded up to 16) in one or two steps
+// ("halves") of N = NP <= 256 columns, each step into the other of two TMEM
+// accumulators, so the epilogue of one step overlaps the MMA of the next and
+// the TMA loads run ahead.  Two halves (G * HP = 2 * NP) use each key tile
+// for twice the tokens, halving the key bytes per flop (measured on GB300,
+// 4096 tokens after 4096: 0.47 -> 0.44 ms).  In the epilogue each thread owns
+// one key row (its TMEM lane) and reduces sum_h w * max(0, D) for each of its
+// tokens in registers -- no cross-thread reduction.
 //
 // Warp roles: warp 0 issues TMA loads (4-stage ring of 32 KB key tiles),
 // warp 1 allocates TMEM and issues MMAs, warps 2..5 stage the queries and run
@@ -28,18 +31,21 @@ namespace dsa {
 namespace {
 
 constexpr int kMaxStages = 4;        // depth of the key-tile ring (runtime: 2..4)
+constexpr int kMaxGroup = 32;        // tokens per group: 2 halves x 256 columns / 16 padded heads
+constexpr size_t kSmemLimit = 232448;   // opt-in shared memory per CTA (227 KB)
 constexpr int kTileKeys = 128;
 constexpr int kTileBytes = kTileKeys * D_I * 2;  // 32 KB: two 64-column SW128 boxes
-// Epilogue warps per CTA: 16 (four per TMEM lane quarter, splitting a
-// group's tokens, one token per TMEM round trip) for multi-token groups --
-// measured on GB300 the epilogue, not the tensor core, bounds prefill
-// scoring, and 16 warps hide its latency better than 8 with two tokens per
-// round trip; 4 (several CTAs per SM) for one-token decode groups.
+// Epilogue warps per CTA: 16 (four per TMEM lane quarter, splitting each
+// step's tokens) for multi-token groups -- measured on GB300 the epilogue
+// needs them to keep pace with the tensor core; 4 (several CTAs per SM) for
+// one-token decode groups.
 template <int kEpi> struct ScoreCfg {
     static constexpr int kEpiWarps = kEpi;
     static constexpr int kThreads = 64 + 32 * kEpi;
-    static constexpr int kTokPerWait = kEpi == 8 ? 2 : 1;
-    static constexpr int kHalves = kEpi / 4;
+    static constexpr int kQuarterWarps = kEpi / 4;   // epilogue warps per TMEM lane quarter
+    // 16-column blocks per TMEM round trip: all 64 heads with registers to
+    // spare (four epilogue warps), 32 heads under the 16-warp register cap
+    static constexpr int kBlocksPerTrip = kEpi == 4 ? 4 : 2;
 };
 
 struct ScoreParams {
@@ -50,7 +56,8 @@ struct ScoreParams {
     DevBatch b;
     uint32_t *status;
     RowMap rows;
-    int H_I, HP, G, NP;       // heads, padded heads, tokens per group, padded N = G*HP
+    int H_I, HP, G;           // heads, padded heads, tokens per group
+    int NQ, NP, halves;       // query operand rows G*HP; MMA N of a step NQ/halves (<= 256); steps per tile
     int hadamard_q;
     int fill_masked;
     int depends;
@@ -68,7 +75,7 @@ struct ScoreParams {
 
 struct Smem {
     uint4 new_key[16];        // the appended key row (fp16, row-major), fused-append mode
-    float4 w4[64];            // head weights of the group's tokens (HP per token)
+    float4 w4[128];           // head weights of the group's tokens (HP per token)
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t acc_full[2];
@@ -78,9 +85,13 @@ struct Smem {
     int32_t abort_flag;
     int32_t meta_q0, meta_q1, meta_max_p;
     int64_t meta_kv0;
-    int32_t pos[256];
-    int64_t out_row[256];
+    int32_t pos[kMaxGroup];
+    int64_t out_row[kMaxGroup];
 };
+
+// Two halves of 256 columns (a 512-row query operand) leave room for a
+// 3-deep ring -- with no slack for realigning the dynamic shared memory.
+static_assert(512 * 256 + 3 * kTileBytes + sizeof(Smem) <= kSmemLimit, "score ring does not fit");
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Smem &sm,
                                          uint32_t *status) {
@@ -98,7 +109,7 @@ __device__ __forceinline__ uint2 load_q_row(const uint16_t *src, bool valid, int
 
 // Rotate (optionally) a query row, split it into fp16 hi (+ lo) parts and
 // store them at row n of the SW128 K-major operand.
-__device__ __forceinline__ void store_q_row(uint2 x, int hadamard, uint8_t *q_hi, uint8_t *q_lo, int NP,
+__device__ __forceinline__ void store_q_row(uint2 x, int hadamard, uint8_t *q_hi, uint8_t *q_lo, int NQ,
                                             int n, int lane) {
     float v[4];
     v[0] = __half2float(__ushort_as_half((unsigned short)(x.x & 0xFFFF)));
@@ -135,7 +146,7 @@ __device__ __forceinline__ void store_q_row(uint2 x, int hadamard, uint8_t *q_hi
     }
     // element 4*lane: K block lane/16, chunk (lane%16)/2, half-chunk lane%2
     const int kb = lane >> 4;
-    const uint32_t off = (uint32_t)kb * (uint32_t)(NP * 128) +
+    const uint32_t off = (uint32_t)kb * (uint32_t)(NQ * 128) +
                          sw128_offset((uint32_t)n, (uint32_t)((lane & 15) >> 1)) + (lane & 1) * 8;
     uint2 o;
     o.x = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
@@ -195,13 +206,19 @@ template <int kEpi>
 __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     score_kernel(const ScoreParams p, const __grid_constant__ CUtensorMap k_map) {
     constexpr int kEpiWarps = ScoreCfg<kEpi>::kEpiWarps;
-    constexpr int kTokPerWait = ScoreCfg<kEpi>::kTokPerWait;
-    constexpr int kHalves = ScoreCfg<kEpi>::kHalves;
+    constexpr int kQuarterWarps = ScoreCfg<kEpi>::kQuarterWarps;
+    constexpr int kBT = ScoreCfg<kEpi>::kBlocksPerTrip;
+    // The operand region (SW128 atoms: 1024-byte aligned) starts the dynamic
+    // shared memory, then the control block.  The launch requests no slack
+    // for realignment (the deepest ring leaves a few hundred bytes of the
+    // 227 KB), so a misaligned window skips the work and says so.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte aligned operand region, then the control block.
-    uint8_t *base = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int q_bytes = p.NP * 256;                      // two 64-column K blocks
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) flag(p.status, DSA_DEV_SMEM_LAYOUT);
+        return;
+    }
+    uint8_t *base = smem_raw;
+    const int q_bytes = p.NQ * 256;                      // two 64-column K blocks
     uint8_t *q_hi = base;
     uint8_t *q_lo = base + q_bytes;                      // used with hadamard_q
     uint8_t *stages = base + q_bytes * (p.hadamard_q ? 2 : 1);
@@ -215,7 +232,10 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
 
     // ---- which tokens and keys this CTA covers (uniform across the CTA)
     const int seq = blockIdx.y / p.groups_per_seq;
-    const int grp = blockIdx.y % p.groups_per_seq;
+    // later groups of a sequence see more keys: launch them first, so that
+    // the last wave holds the shortest CTAs (measured on GB300, 4096 tokens
+    // after 4096: 3% off the scoring)
+    const int grp = p.groups_per_seq - 1 - (int)(blockIdx.y % p.groups_per_seq);
     if (seq >= b.B) return;
     if (threadIdx.x == 0) {                       // three independent loads
         sm.meta_q0 = __ldg(b.cu_q + seq);
@@ -236,6 +256,8 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     const int j_hi = min(j_lo + p.G, win_hi);
     if (j_lo >= j_hi) return;
     const int g = j_hi - j_lo;
+    const int tph = p.G / p.halves;               // tokens per half
+    const int hv = (p.halves == 2 && g > tph) ? 2 : 1;   // MMA steps per tile
     if ((int)threadIdx.x < g) {                   // the group's positions, in parallel
         const int i = threadIdx.x;
         const int t = q0 + j_lo + i;
@@ -341,47 +363,79 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
             tc_fence_after();
             const uint32_t idesc = idesc_f16(128, p.NP, false, false, false);
             const uint32_t qh = smem_u32(q_hi), ql = smem_u32(q_lo);
-            const uint32_t qblk = (uint32_t)p.NP * 128u;
-            for (int i = 0; i < n_mma; ++i) {
-                const int s = i % n_stages;
-                const uint32_t k = (uint32_t)(i / n_stages);
-                const int buf = i & 1;
-                const uint32_t ka = (uint32_t)(i >> 1);
-                if (!wait_bar(smem_u32(&sm.acc_empty[buf]), (ka & 1) ^ 1, sm, p.status)) break;
-                if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status)) break;
-                tc_fence_after();
-                if (i == append_tile) {
-                    // replace the stale cache row loaded by TMA with the new key
-                    const uint32_t r = (uint32_t)(max_p - (chunk0 + (int64_t)i * kTileKeys));
-                    uint8_t *tile = stages + s * kTileBytes;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTileBytes / 2) + sw128_offset(r, c & 7)) =
-                            sm.new_key[c];
-                    fence_proxy_async_smem();
-                }
-                const uint32_t d = tmem + (uint32_t)(buf * p.NP);
-                const uint32_t a0 = smem_u32(stages + s * kTileBytes);
+            const uint32_t qblk = (uint32_t)p.NQ * 128u;
+            // the 8 (16 with the lo query part) MMAs of one step: keys of stage
+            // buffer a0 against query rows [qrow0, qrow0 + NP) into column d
+            auto issue_step = [&](uint32_t d, uint32_t a0, uint32_t qrow0) {
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t koff = (uint32_t)(kb * (kTileBytes / 2) + ks * 32);
                         const uint64_t ad = sdesc_sw128(a0 + koff, 16, 1024);
-                        const uint32_t boff = (uint32_t)kb * qblk + (uint32_t)ks * 32;
+                        const uint32_t boff = (uint32_t)kb * qblk + qrow0 * 128u + (uint32_t)ks * 32;
                         umma_f16(d, ad, sdesc_sw128(qh + boff, 16, 1024), idesc, (kb | ks) != 0);
                         if (p.hadamard_q) umma_f16(d, ad, sdesc_sw128(ql + boff, 16, 1024), idesc, 1);
                     }
                 }
-                umma_commit(smem_u32(&sm.empty[s]));
-                umma_commit(smem_u32(&sm.acc_full[buf]));
+            };
+            // replace the stale cache row loaded by TMA with the new key
+            auto patch_append = [&](int i, int s) {
+                const uint32_t r = (uint32_t)(max_p - (chunk0 + (int64_t)i * kTileKeys));
+                uint8_t *tile = stages + s * kTileBytes;
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<uint4 *>(tile + (c >> 3) * (kTileBytes / 2) + sw128_offset(r, c & 7)) =
+                        sm.new_key[c];
+                fence_proxy_async_smem();
+            };
+            if constexpr (kEpi == 4) {
+                // one token: one step per tile, the stage released before the
+                // accumulator is signalled (measured on GB300, ragged
+                // long-context decode: 7 us per step faster than the general loop)
+                for (int i = 0; i < n_mma; ++i) {
+                    const int s = i % n_stages;
+                    const uint32_t k = (uint32_t)(i / n_stages);
+                    const int buf = i & 1;
+                    const uint32_t ka = (uint32_t)(i >> 1);
+                    if (!wait_bar(smem_u32(&sm.acc_empty[buf]), (ka & 1) ^ 1, sm, p.status)) break;
+                    if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status)) break;
+                    tc_fence_after();
+                    if (i == append_tile) patch_append(i, s);
+                    issue_step(tmem + (uint32_t)(buf * p.NP), smem_u32(stages + s * kTileBytes), 0);
+                    umma_commit(smem_u32(&sm.empty[s]));
+                    umma_commit(smem_u32(&sm.acc_full[buf]));
+                }
+            } else {
+                for (int i = 0; i < n_mma; ++i) {
+                    const int s = i % n_stages;
+                    const uint32_t k = (uint32_t)(i / n_stages);
+                    if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status)) break;
+                    tc_fence_after();
+                    if (i == append_tile) patch_append(i, s);
+                    const uint32_t a0 = smem_u32(stages + s * kTileBytes);
+                    bool ok = true;
+#pragma unroll 1
+                    for (int h = 0; h < hv; ++h) {
+                        const uint32_t u = (uint32_t)(i * hv + h);   // MMA step: accumulator u & 1
+                        if (!wait_bar(smem_u32(&sm.acc_empty[u & 1]), ((u >> 1) & 1) ^ 1, sm, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_step(tmem + (u & 1) * (uint32_t)p.NP, a0, (uint32_t)(h * p.NP));
+                        umma_commit(smem_u32(&sm.acc_full[u & 1]));
+                    }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&sm.empty[s]));   // the tile's last MMA step read it
+                }
             }
         }
     } else {
         // ---------------- query staging + epilogue
         const int ew = warp - 2;  // 0..kEpiWarps-1
         // stage weights
-        for (int i = threadIdx.x - 64; i < p.G * p.HP; i += 32 * kEpiWarps) {
+        for (int i = threadIdx.x - 64; i < p.NQ; i += 32 * kEpiWarps) {
             const int tok = i / p.HP, h = i % p.HP;
             float wv = 0.f;
             if (tok < g && h < p.H_I && sm.pos[tok] >= 0)
@@ -389,20 +443,20 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
             reinterpret_cast<float *>(sm.w4)[i] = wv;
         }
         // stage query rows n = tok*HP + h; each warp keeps 8 row loads in flight
-        for (int n0 = ew; n0 < p.NP; n0 += 8 * kEpiWarps) {
+        for (int n0 = ew; n0 < p.NQ; n0 += 8 * kEpiWarps) {
             uint2 x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int n = n0 + u * kEpiWarps;
                 const int tok = n / p.HP, h = n % p.HP;
-                const bool valid = n < p.NP && tok < g && h < p.H_I;
+                const bool valid = n < p.NQ && tok < g && h < p.H_I;
                 x[u] = load_q_row(p.q_idx + ((int64_t)(q0 + j_lo + (valid ? tok : 0)) * p.H_I + (valid ? h : 0)) * D_I,
                                   valid, lane);
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int n = n0 + u * kEpiWarps;
-                if (n < p.NP) store_q_row(x[u], p.hadamard_q, q_hi, q_lo, p.NP, n, lane);
+                if (n < p.NQ) store_q_row(x[u], p.hadamard_q, q_hi, q_lo, p.NQ, n, lane);
             }
         }
         fence_proxy_async_smem();
@@ -411,70 +465,71 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         if (lane == 0) mbar_arrive(smem_u32(&sm.q_ready));
 
         const int quarter = warp & 3;         // TMEM lanes this warp may access
-        const int half = ew >> 2;             // which part of the group's tokens
+        const int part = ew >> 2;             // which part of each half's tokens
         const int r = quarter * 32 + lane;    // key row within a tile
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int hp16 = p.HP >> 4;
-        const int tpw = (g + kHalves - 1) / kHalves;
-        const int tok_lo = min(g, half * tpw), tok_hi = min(g, tok_lo + tpw);
-        for (int i = 0; i < n_tiles; ++i) {
+        const int tpw = (tph + kQuarterWarps - 1) / kQuarterWarps;
+        const int lo_h = min(tph, part * tpw), hi_h = min(tph, lo_h + tpw);   // within a half
+        bool aborted = false;
+        const uint32_t n_steps = (uint32_t)(n_mma * hv);
+        for (uint32_t u = 0; u < n_steps; ++u) {     // MMA step u: tile u / hv, half u % hv, accumulator u & 1
+            const int i = hv == 2 ? (int)(u >> 1) : (int)u;
+            const int h = (int)u & (hv - 1);
             const int64_t s = chunk0 + (int64_t)i * kTileKeys + r;
-            if (i < n_mma) {
-                const int buf = i & 1;
-                const uint32_t ka = (uint32_t)(i >> 1);
-                if (!wait_bar(smem_u32(&sm.acc_full[buf]), ka & 1, sm, p.status)) break;
-                tc_fence_after();
-                // two tokens' accumulators per TMEM round trip
-                for (int tok = tok_lo; tok < tok_hi; tok += kTokPerWait) {
-                    const bool two = kTokPerWait == 2 && tok + 1 < tok_hi;
-                    const uint32_t col = tmem + lane_addr + (uint32_t)(buf * p.NP + tok * p.HP);
-                    uint32_t v[4 * kTokPerWait][16];
+            const int buf = (int)(u & 1);
+            if (!wait_bar(smem_u32(&sm.acc_full[buf]), (u >> 1) & 1, sm, p.status)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const int tok_lo = min(g, h * tph + lo_h), tok_hi = min(g, h * tph + hi_h);
+            // kBT 16-column loads per TMEM round trip, accumulated in head order
+            for (int tok = tok_lo; tok < tok_hi; ++tok) {
+                const uint32_t col = tmem + lane_addr + (uint32_t)(buf * p.NP + (tok - h * tph) * p.HP);
+                const float4 *wt = sm.w4 + (tok * p.HP >> 2);   // broadcast 16-byte loads
+                float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (c < hp16) tmem_ld16(col + 16 * c, v[c]);
-                    if constexpr (kTokPerWait == 2) {
-                        if (two) {
+                for (int c0 = 0; c0 < 4; c0 += kBT) {
+                    if (c0 < hp16) {
+                        uint32_t v[kBT][16];
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                if (c < hp16) tmem_ld16(col + p.HP + 16 * c, v[4 + c]);
-                        }
-                    }
-                    tmem_wait_ld();
+                        for (int c = 0; c < kBT; ++c)
+                            if (c0 + c < hp16) tmem_ld16(col + 16 * (c0 + c), v[c]);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < kTokPerWait; ++u) {
-                        if (u == 1 && !two) break;
-                        const int tk = tok + u;
-                        const float4 *wt = sm.w4 + (tk * p.HP >> 2);   // broadcast 16-byte loads
-                        float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            if (c < hp16) {
+                        for (int c = 0; c < kBT; ++c) {
+                            if (c0 + c < hp16) {
 #pragma unroll
                                 for (int j = 0; j < 16; j += 4) {
-                                    const float4 w = wt[4 * c + (j >> 2)];
-                                    const float2 r01 = make_float2(fmaxf(__uint_as_float(v[4 * u + c][j]), 0.f),
-                                                                   fmaxf(__uint_as_float(v[4 * u + c][j + 1]), 0.f));
-                                    const float2 r23 = make_float2(fmaxf(__uint_as_float(v[4 * u + c][j + 2]), 0.f),
-                                                                   fmaxf(__uint_as_float(v[4 * u + c][j + 3]), 0.f));
+                                    const float4 w = wt[4 * (c0 + c) + (j >> 2)];
+                                    const float2 r01 = make_float2(fmaxf(__uint_as_float(v[c][j]), 0.f),
+                                                                   fmaxf(__uint_as_float(v[c][j + 1]), 0.f));
+                                    const float2 r23 = make_float2(fmaxf(__uint_as_float(v[c][j + 2]), 0.f),
+                                                                   fmaxf(__uint_as_float(v[c][j + 3]), 0.f));
                                     acc2 = __ffma2_rn(make_float2(w.x, w.y), r01, acc2);
                                     acc2 = __ffma2_rn(make_float2(w.z, w.w), r23, acc2);
                                 }
                             }
                         }
-                        const float acc = acc2.x + acc2.y;
-                        const int pos = sm.pos[tk];
-                        float *dst = p.scores + sm.out_row[tk] * p.ld;
-                        if (s <= pos) dst[s] = acc;
-                        else if (p.fill_masked && s < p.ld) dst[s] = -INFINITY;
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
-            } else {
-                for (int tok = tok_lo; tok < tok_hi; ++tok)
-                    if (s < p.ld) p.scores[sm.out_row[tok] * p.ld + s] = -INFINITY;
+                const float acc = acc2.x + acc2.y;
+                const int pos = sm.pos[tok];
+                float *dst = p.scores + sm.out_row[tok] * p.ld;
+                if (s <= pos) dst[s] = acc;
+                else if (p.fill_masked && s < p.ld) dst[s] = -INFINITY;
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
+        }
+        // tiles beyond every token's position (fill_masked)
+        for (int i = n_mma; i < n_tiles && !aborted; ++i) {
+            const int64_t s = chunk0 + (int64_t)i * kTileKeys + r;
+            for (int h = 0; h < hv; ++h)
+                for (int tok = min(g, h * tph + lo_h); tok < min(g, h * tph + hi_h); ++tok)
+                    if (s < p.ld) p.scores[sm.out_row[tok] * p.ld + s] = -INFINITY;
         }
     }
 
@@ -488,9 +543,8 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     }
 }
 
-size_t score_smem_bytes(int n_pad, int hadamard_q, int n_stages) {
-    return 1024 + (size_t)n_pad * 256 * (hadamard_q ? 2 : 1) + (size_t)n_stages * kTileBytes +
-           sizeof(Smem);
+size_t score_smem_bytes(int n_rows, int hadamard_q, int n_stages) {
+    return (size_t)n_rows * 256 * (hadamard_q ? 2 : 1) + (size_t)n_stages * kTileBytes + sizeof(Smem);
 }
 
 cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const DevBatch &b,
@@ -505,10 +559,17 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     p.rows = a.rows;
     p.H_I = a.H_I;
     p.HP = (a.H_I + 15) / 16 * 16;
-    const int n_max = a.hadamard_q ? 128 : 256;
+    const int n_max = a.hadamard_q ? 128 : 256;             // MMA N of one step
     const int window = a.rows.slab ? a.rows.J : b.max_q;
-    p.G = max(1, min(n_max / p.HP, window));
-    p.NP = p.G * p.HP;
+    const int g1 = max(1, min(n_max / p.HP, window));       // tokens per step
+    // Multi-token groups without the rotation's second (lo) operand take two
+    // steps per key tile; with it the doubled query operand would not leave
+    // room for the ring.
+    p.halves = (!a.hadamard_q && g1 > 1 && window > g1) ? 2 : 1;
+    p.G = g1 * p.halves;
+    p.NP = g1 * p.HP;
+    p.NQ = p.G * p.HP;
+    if (p.G > kMaxGroup) return cudaErrorInvalidConfiguration;
     p.hadamard_q = a.hadamard_q;
     p.fill_masked = a.fill_masked;
     p.depends = a.depends;
@@ -534,12 +595,14 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     // long-context decode, 90 us against 128 us with a 4-deep ring at one CTA
     // per SM.
     p.stages = (p.G == 1 || tpc <= 2) ? 2 : kMaxStages;
+    while (p.stages > 2 && score_smem_bytes(p.NQ, p.hadamard_q, p.stages) > kSmemLimit) --p.stages;
     const int64_t chunks = (tiles + tpc - 1) / tpc;
     const int64_t groups = (int64_t)b.B * p.groups_per_seq;
     if (groups > 65535 || chunks > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
-    const size_t smem = score_smem_bytes(p.NP, p.hadamard_q, p.stages);
-    const size_t smem_max = std::min<size_t>(232448, score_smem_bytes(256, 1, kMaxStages));
+    const size_t smem = score_smem_bytes(p.NQ, p.hadamard_q, p.stages);
+    if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
+    const size_t smem_max = kSmemLimit;
     dim3 grid((unsigned)chunks, (unsigned)groups);
     // One wave of this kernel (decode variant: two CTAs per SM) followed by a
     // small dependent grid: that grid can start on the SMs left free.

@@ -77,7 +77,8 @@ typedef enum {
 enum {
     DSA_DEV_BAD_POSITION = 1u << 0, /* q_pos / kv_off / cu_q outside the stated bounds */
     DSA_DEV_BAD_INDEX    = 1u << 1, /* an idx entry not in {-1} U [0, q_pos[t]] */
-    DSA_DEV_TIMEOUT      = 1u << 2  /* a bounded wait on an mbarrier gave up */
+    DSA_DEV_TIMEOUT      = 1u << 2, /* a bounded wait on an mbarrier gave up */
+    DSA_DEV_SMEM_LAYOUT  = 1u << 3  /* a kernel found its shared memory not 1024-byte aligned (work skipped) */
 };
 
 /* dtype of new indexer keys */

@@ -68,6 +68,10 @@ SCORE_CASES = [
     ("decode_HI64_rot", dict(lengths=[1500, 256, 90]), 64, True),
     ("decode_HI48", dict(lengths=[640, 1025]), 48, False),
     ("prefill_HI64", dict(cached=500, T=70), 64, False),
+    # two MMA steps per key tile; each last group takes one (g <= tokens per step)
+    ("prefill_HI64_tail2", dict(cached=200, T=10), 64, False),
+    ("prefill_HI16", dict(cached=700, T=45), 16, False),
+    ("prefill_HI48", dict(cached=333, T=23), 48, False),
     ("prefill_HI16_rot", dict(cached=300, T=37), 16, True),
     ("prefill_HI32_rot", dict(cached=1000, T=9), 32, True),
 ]
