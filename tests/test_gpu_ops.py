@@ -131,6 +131,10 @@ def _topk_case(kind, rng):
         L, pos = 20000, [19999, 12000, 8191, 8192, 3000, 100]
         s = rng.standard_normal((len(pos), L)).astype(np.float32)
         s[:, 5000:5100] = 0.5                   # a run of ties inside one CTA's share
+    elif kind in ("cluster5", "cluster7"):      # cluster sizes that do not divide the histogram
+        L = 70000 if kind == "cluster5" else 110000
+        pos = [L - 1, L // 2, 16384, 16383, 5000]
+        s = (rng.integers(-64, 64, (len(pos), L)) * 2.0 ** -6).astype(np.float32)   # many ties
     elif kind == "beyond_cluster":              # longer than a cluster holds: shared-memory path
         L, pos = 140000, [139999, 131072]
         s = rng.standard_normal((len(pos), L)).astype(np.float32)
@@ -143,7 +147,7 @@ def _topk_case(kind, rng):
 
 
 @pytest.mark.parametrize("kind", ["random", "ties", "all_equal", "signed_zero", "neg_inf", "long_row", "narrow",
-                                  "cluster3", "beyond_cluster"])
+                                  "cluster3", "cluster5", "cluster7", "beyond_cluster"])
 @pytest.mark.parametrize("k", [1, 2048])
 def test_topk_bit_exact_on_oracle_scores(dsa, kind, k):
     import torch
