@@ -43,7 +43,8 @@
  *  - Host validation runs before anything is enqueued; a failing call
  *    enqueues nothing.  A failed launch returns DSA_ERR_CUDA.
  *  - Device-detected problems (a position outside the stated bounds, an
- *    index out of range, a bounded wait that gave up) never trap: the kernel
+ *    index out of range, a bounded wait that gave up, shared memory that is
+ *    not aligned as a kernel laid it out) never trap: the kernel
  *    skips the offending work, ORs a DSA_DEV_* bit into the status word at
  *    the start of the workspace and carries on.  dsa_read_device_status
  *    reads and clears it.

@@ -36,6 +36,16 @@ def test_exports_every_declared_symbol(L):
     assert set(declared()) == set(dsa.SIGNATURES), "binding and header disagree"
 
 
+def test_device_status_bits_match_the_header():
+    """The binding's DSA_DEV_* constants are the header's enum values."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    bits = {name: 1 << int(sh) for name, sh in re.findall(r"\b(DSA_DEV_[A-Z_]+)\s*=\s*1u\s*<<\s*(\d+)", src)}
+    assert len(bits) >= 4
+    for name, value in bits.items():
+        assert getattr(dsa, name) == value, name
+    assert len(set(bits.values())) == len(bits), "bits overlap"
+
+
 def test_version_and_status_strings(L):
     assert dsa.dsa_version() == 10000
     for code in range(0, 7):
