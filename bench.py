@@ -186,6 +186,29 @@ def max_over_ranks(x: float) -> float:
     return float(t.item())
 
 
+def stage_split(t, pairs):
+    """Per-stage milliseconds of one traced step.
+
+    t: elapsed ms from trace event 0 to events 1..5 (before the first score,
+    before the first top-k, before the attention, before the combine, after
+    the last launch).  pairs: elapsed ms to events (6 + 2j, 7 + 2j), which
+    bracket the top-k of score window j; a pair outside [t[0], t[2]] is a
+    slot this call did not record, and ends the windows.  With several
+    windows the score stage is everything between the append and the
+    attention that is not top-k.
+    """
+    win = []
+    for a, b in pairs:
+        if not (t[0] <= a <= b <= t[2]):
+            break
+        win.append((a, b))
+    if not win:
+        win = [(t[1], t[2])]
+    topk = sum(b - a for a, b in win)
+    return {"k_append": t[0], "indexer_score": t[2] - t[0] - topk, "topk": topk,
+            "sparse_attn": t[3] - t[2], "attn_combine": t[4] - t[3]}
+
+
 def job_throughput(world: int, tokens_per_step: int, steps: int, seconds: float) -> float:
     """Whole-job tokens per second: every rank runs its own replica of the
     workload (weak scaling), so the job processes world x tokens per step."""
@@ -592,22 +615,10 @@ def main():
         run_traced()
         trace[5].synchronize()
         t = [trace[0].elapsed_time(trace[j]) for j in range(1, 6)]
-        # windows: the top-k of window j sits between events 6+2j and 7+2j;
-        # slots of windows this call does not have hold older timestamps
-        win = []
-        for j in range(MAX_TRACE_WINDOWS):
-            a, b = trace[0].elapsed_time(trace[6 + 2 * j]), trace[0].elapsed_time(trace[7 + 2 * j])
-            if not (t[0] <= a <= b <= t[2]):
-                break
-            win.append((a, b))
-        if not win:
-            win = [(t[1], t[2])]
-        topk = sum(b - a for a, b in win)
-        stage_ms["k_append"].append(t[0])
-        stage_ms["indexer_score"].append(t[2] - t[0] - topk)
-        stage_ms["topk"].append(topk)
-        stage_ms["sparse_attn"].append(t[3] - t[2])
-        stage_ms["attn_combine"].append(t[4] - t[3])
+        pairs = [(trace[0].elapsed_time(trace[6 + 2 * j]), trace[0].elapsed_time(trace[7 + 2 * j]))
+                 for j in range(MAX_TRACE_WINDOWS)]
+        for s_, v in stage_split(t, pairs).items():
+            stage_ms[s_].append(v)
     # the step with the device timeline: per-kernel [start, end] inside a step
     tl = {s: [] for s in STAGES}
     big = torch.iinfo(torch.int64).max
