@@ -36,6 +36,8 @@ def lib():
             "oracle_topk": (I32, [P, I64, I32, P, I32, P]),
             "oracle_sparse_attn_f64": (I32, [P, P, P, I32, I32, P, P, P, P, I32, I32, F64, P, P]),
             "oracle_sparse_attn": (I32, [P, P, P, I32, I32, P, P, P, P, I32, I32, F64, P, P]),
+            "oracle_sparse_attn_nope_f64": (I32, [P, P, I32, I32, P, P, P, P, I32, I32, F64, P, P]),
+            "oracle_sparse_attn_nope": (I32, [P, P, I32, I32, P, P, P, P, I32, I32, F64, P, P]),
             "oracle_dense_attn_f64": (I32, [P, P, P, I32, I32, P, P, P, I32, F64, P, P]),
             "oracle_unabsorbed_attn": (I32, [P, P, P, I32, I32, P, P, P, P, P, P, I32, I32, F64, P]),
             "oracle_decode": (I32, [P, I32, P, P, P, P, P, P, I32, I32, P, P, P, I32, I32, I32, F64,
@@ -185,6 +187,33 @@ def sparse_attn_f64(q_lat, q_rope, kv_cache, batch: Batch, idx, sm_scale: float)
     _check(lib().oracle_sparse_attn_f64(_p(ql), _p(qr), _p(_c(kv_cache, np.uint16)), *batch.args(),
                                         _p(ix), ix.shape[1], H, sm_scale, _p(out), _p(lse)),
            "sparse_attn_f64")
+    return out, lse
+
+
+def sparse_attn_nope(q_lat, kv_latent, batch: Batch, idx, sm_scale: float):
+    """MLA-NoPE (no rope tail; vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on
+    gfx1030"): bf16-bit queries [T,H,512] against bf16-bit latent rows
+    [rows,512].  Returns (out [T,H,512], lse [T,H]) in float64."""
+    ql = _c(q_lat, np.uint16)
+    T, H, _ = ql.shape
+    ix = _c(idx, np.int32)
+    out = np.empty((T, H, 512), np.float64)
+    lse = np.empty((T, H), np.float64)
+    _check(lib().oracle_sparse_attn_nope(_p(ql), _p(_c(kv_latent, np.uint16)), *batch.args(),
+                                         _p(ix), ix.shape[1], H, sm_scale, _p(out), _p(lse)),
+           "sparse_attn_nope")
+    return out, lse
+
+
+def sparse_attn_nope_f64(q_lat, kv_latent, batch: Batch, idx, sm_scale: float):
+    ql = _c(q_lat, np.float64)
+    T, H, _ = ql.shape
+    ix = _c(idx, np.int32)
+    out = np.empty((T, H, 512), np.float64)
+    lse = np.empty((T, H), np.float64)
+    _check(lib().oracle_sparse_attn_nope_f64(_p(ql), _p(_c(kv_latent, np.uint16)), *batch.args(),
+                                             _p(ix), ix.shape[1], H, sm_scale, _p(out), _p(lse)),
+           "sparse_attn_nope_f64")
     return out, lse
 
 

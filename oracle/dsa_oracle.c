@@ -322,6 +322,74 @@ int oracle_sparse_attn(const uint16_t *q_lat, const uint16_t *q_rope, const uint
     return rc;
 }
 
+/* One (token, head) of the NoPE form: rows of D_L latent values only. */
+static void attend_rows_nope(const double *ql, const uint16_t *kv_latent, int64_t base,
+                             const int32_t *pos, int n, double sm_scale, double *o, double *lse)
+{
+    for (int d = 0; d < D_L; d++) o[d] = 0.0;
+    if (n == 0) { if (lse) *lse = -INFINITY; return; }
+    double *z = malloc(sizeof(double) * (size_t)n);
+    double m = -INFINITY;
+    for (int j = 0; j < n; j++) {
+        const uint16_t *c = kv_latent + (base + pos[j]) * (int64_t)D_L;
+        double acc = 0.0;
+        for (int d = 0; d < D_L; d++) acc += ql[d] * oracle_bf16_to_f64(c[d]);
+        z[j] = sm_scale * acc;
+        if (z[j] > m) m = z[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j < n; j++) {
+        double p = exp(z[j] - m);
+        l += p;
+        const uint16_t *c = kv_latent + (base + pos[j]) * (int64_t)D_L;
+        for (int d = 0; d < D_L; d++) o[d] += p * oracle_bf16_to_f64(c[d]);
+    }
+    for (int d = 0; d < D_L; d++) o[d] /= l;
+    if (lse) *lse = m + log(l);
+    free(z);
+}
+
+int oracle_sparse_attn_nope_f64(const double *q_lat, const uint16_t *kv_latent,
+                                int B, int T, const int32_t *cu_q, const int32_t *q_pos,
+                                const int64_t *kv_off, const int32_t *idx, int k, int H,
+                                double sm_scale, double *out, double *lse)
+{
+    if (check_batch(B, T, cu_q, q_pos) || k < 1 || H < 1) return -1;
+    for (int t = 0; t < T; t++)
+        for (int i = 0; i < k; i++) {
+            int32_t j = idx[(int64_t)t * k + i];
+            if (j != -1 && (j < 0 || j > q_pos[t])) return -2;
+        }
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int t = 0; t < T; t++)
+        for (int h = 0; h < H; h++) {
+            int b = seq_of(t, B, cu_q);
+            int32_t *pos = malloc(sizeof(int32_t) * (size_t)k);
+            int n = 0;
+            for (int i = 0; i < k; i++) {
+                int32_t j = idx[(int64_t)t * k + i];
+                if (j >= 0) pos[n++] = j;
+            }
+            attend_rows_nope(q_lat + ((int64_t)t * H + h) * D_L, kv_latent, kv_off[b], pos, n, sm_scale,
+                             out + ((int64_t)t * H + h) * D_L, lse ? lse + (int64_t)t * H + h : NULL);
+            free(pos);
+        }
+    return 0;
+}
+
+int oracle_sparse_attn_nope(const uint16_t *q_lat, const uint16_t *kv_latent,
+                            int B, int T, const int32_t *cu_q, const int32_t *q_pos,
+                            const int64_t *kv_off, const int32_t *idx, int k, int H,
+                            double sm_scale, double *out, double *lse)
+{
+    double *ql = bf16_array_to_f64(q_lat, (int64_t)T * H * D_L);
+    int rc = ql ? oracle_sparse_attn_nope_f64(ql, kv_latent, B, T, cu_q, q_pos, kv_off, idx, k, H,
+                                              sm_scale, out, lse)
+                : -1;
+    free(ql);
+    return rc;
+}
+
 int oracle_dense_attn_f64(const double *q_lat, const double *q_rope, const uint16_t *kv_cache,
                           int B, int T, const int32_t *cu_q, const int32_t *q_pos,
                           const int64_t *kv_off, int H, double sm_scale,

@@ -75,6 +75,24 @@ int oracle_sparse_attn(const uint16_t *q_lat, const uint16_t *q_rope, const uint
                        const int64_t *kv_off, const int32_t *idx, int k, int H,
                        double sm_scale, double *out, double *lse);
 
+/* MLA-NoPE sparse attention (vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on
+ * gfx1030", DSA = MLA-NoPE: the 512-d kv latent is cached per token and no
+ * RoPE is applied anywhere), in the absorbed (latent) form:
+ *   z_j = sm_scale * q_lat[t,h] . c_j[0:512],
+ *   o[t,h] = sum_j softmax(z)_j * c_j,  lse[t,h] = log sum_j exp(z_j)
+ * over j in idx[t, 0:k) as for oracle_sparse_attn_f64.  kv_latent bf16
+ * [rows,512]; q_lat double [T,H,512]; out double [T,H,512]; lse may be NULL. */
+int oracle_sparse_attn_nope_f64(const double *q_lat, const uint16_t *kv_latent,
+                                int B, int T, const int32_t *cu_q, const int32_t *q_pos,
+                                const int64_t *kv_off, const int32_t *idx, int k, int H,
+                                double sm_scale, double *out, double *lse);
+
+/* Same with bf16 queries. */
+int oracle_sparse_attn_nope(const uint16_t *q_lat, const uint16_t *kv_latent,
+                            int B, int T, const int32_t *cu_q, const int32_t *q_pos,
+                            const int64_t *kv_off, const int32_t *idx, int k, int H,
+                            double sm_scale, double *out, double *lse);
+
 /* Dense causal MLA attention (absorbed form): softmax over every s <= q_pos[t]. */
 int oracle_dense_attn_f64(const double *q_lat, const double *q_rope, const uint16_t *kv_cache,
                           int B, int T, const int32_t *cu_q, const int32_t *q_pos,
