@@ -61,6 +61,7 @@ SIGNATURES = {
     "dsa_topk": (_I, [_P, _I64, _BP, _I, _P, _P, _SZ, _P]),
     "dsa_topk_sink": (_I, [_P, _I64, _BP, _I, _I, _P, _P, _P, _SZ, _P]),
     "dsa_sparse_mla_attn": (_I, [_P, _P, _P, _BP, _P, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "dsa_sparse_mla_attn_nope": (_I, [_P, _P, _BP, _P, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "dsa_decode": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _P, _P, _P, _P, _SZ, _P]),
     "dsa_decode_sink": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _BP, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _P,
                              _SZ, _P]),
@@ -254,6 +255,20 @@ def dsa_sparse_mla_attn(q_lat, q_rope, kv_cache, batch: Batch, idx, sm_scale: fl
     _check(lib().dsa_sparse_mla_attn(_ptr(q_lat), _ptr(q_rope), _ptr(kv_cache), C.byref(d), _ptr(idx),
                                      idx.shape[1], q_lat.shape[1], sm_scale, _ptr(out), _ptr(lse),
                                      _ptr(ws), ws.numel(), _stream(stream)), "dsa_sparse_mla_attn")
+
+
+def dsa_sparse_mla_attn_nope(q_lat, kv_latent, batch: Batch, idx, sm_scale: float, out, lse, ws, stream=None):
+    """MLA-NoPE: q_lat [T,H,512] against latent rows kv_latent [rows,512] (no rope tail)."""
+    import torch
+    _req(q_lat, torch.bfloat16, "q_lat")
+    _req(kv_latent, torch.bfloat16, "kv_latent")
+    _req(idx, torch.int32, "idx")
+    _req(out, torch.float32, "out")
+    _req(lse, torch.float32, "lse")
+    d = batch.desc()
+    _check(lib().dsa_sparse_mla_attn_nope(_ptr(q_lat), _ptr(kv_latent), C.byref(d), _ptr(idx), idx.shape[1],
+                                          q_lat.shape[1], sm_scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                          _stream(stream)), "dsa_sparse_mla_attn_nope")
 
 
 def dsa_decode(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch: Batch, k: int, sm_scale: float,

@@ -167,7 +167,7 @@ inline void trace(int i, cudaStream_t s) {
 dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const dsa_bf16 *kv_cache,
                            const dsa_batch_t *batch, const int32_t *idx, int k, int H, float sm_scale,
                            float *out, float *lse, void *ws, const Layout &L, cudaStream_t stream,
-                           bool traced, bool pdl, const dsa_paging_t *paging = nullptr) {
+                           bool traced, bool pdl, const dsa_paging_t *paging = nullptr, bool rope = true) {
     DevBatch db = dev_batch(batch);
     if (paging) {
         db.block_table = paging->block_table;
@@ -176,11 +176,15 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
     }
     CUtensorMap ql, qr, kv;
     const uint64_t qrows = (uint64_t)batch->total_q * H;
+    // without the rope tail the latent rows are D_L wide and the kernel never
+    // reads the rope-query map (it gets the latent one)
     if (!make_map(&ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_lat, D_L, qrows, 64, 64) ||
-        !make_map(&qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_rope, D_R, qrows, 64, 64) ||
-        !make_map(&kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv_cache, D_ROW, (uint64_t)batch->cache_rows, 64, 1))
+        !make_map(&qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rope ? q_rope : q_lat, rope ? D_R : D_L, qrows, 64, 64) ||
+        !make_map(&kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv_cache, rope ? D_ROW : D_L,
+                  (uint64_t)batch->cache_rows, 64, 1))
         return DSA_ERR_CUDA;
     AttnLaunch a{};
+    a.rope = rope ? 1 : 0;
     a.H = H;
     a.k = k;
     a.sm_scale = sm_scale;
@@ -355,6 +359,24 @@ dsa_status_t dsa_topk_sink(const float *scores, int64_t ld_scores, const dsa_bat
                            const int32_t *sink_pos0, int32_t *idx, void *ws, size_t ws_bytes,
                            cudaStream_t stream) {
     return topk_impl(scores, ld_scores, batch, k, n_sink, sink_pos0, idx, ws, ws_bytes, stream);
+}
+
+dsa_status_t dsa_sparse_mla_attn_nope(const dsa_bf16 *q_lat, const dsa_bf16 *kv_latent,
+                                      const dsa_batch_t *batch, const int32_t *idx, int k, int H,
+                                      float sm_scale, float *out, float *lse, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!q_lat || !kv_latent || !idx || !out) return DSA_ERR_INVALID_ARGUMENT;
+    if (H < 1 || H > 64 || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    if ((int64_t)batch->total_q * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    if (!aligned(q_lat, 16) || !aligned(kv_latent, 16) || !aligned(out, 16) || !aligned(idx, 4) ||
+        (lse && !aligned(lse, 4)))
+        return DSA_ERR_MISALIGNED;
+    const Layout L = layout(DSA_OP_SPARSE_ATTN, batch, k);
+    if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
+    return run_attention(q_lat, nullptr, kv_latent, batch, idx, k, H, sm_scale, out, lse, ws, L, stream,
+                         false, false, nullptr, false);
 }
 
 dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const dsa_bf16 *kv_cache,

@@ -108,6 +108,7 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
                         const int32_t *sink_pos0 = nullptr);
 
 struct AttnLaunch {
+    int rope = 1;            // 0: 512-wide latent rows without the rope tail
     int H, k;
     float sm_scale;
     const int32_t *idx;      // [T, k]

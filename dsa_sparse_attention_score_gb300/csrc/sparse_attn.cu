@@ -14,7 +14,10 @@
 //     S^T[row, head]  = C[row, 0:576] . Q[head, 0:576]^T        (M=64, N=64, K=576)
 //     O^T[dim, head] += C[row, dim]^T . P^T[row, head]           (M=4x128, N=64, K=64)
 // A gathered tile C sits in shared memory as nine 64-column SWIZZLE_128B
-// blocks (TMA tile::gather4, four rows per request).  The same bytes serve as
+// blocks (TMA tile::gather4, four rows per request).  Without a rope tail
+// (MLA-NoPE: vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on gfx1030", 512-d
+// latent rows) eight blocks are gathered and multiplied, and the ninth only
+// holds P^T.  The same bytes serve as
 // the K-major A operand of S^T and, for the latent blocks, as the MN-major A
 // operand of O^T, so V is never copied.  The rope block is dead once S^T is
 // computed and holds P^T (bf16) for the second MMA.
@@ -67,6 +70,7 @@ struct AttnParams {
     int H, k;
     float scale_log2;        // sm_scale * log2(e)
     int tiles_per_cta, n_split, n_tiles;
+    int rope;                // 1: 576-wide rows with the rope tail; 0: 512-wide latent rows
 };
 
 struct Ctl {
@@ -196,17 +200,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp > kMmaWarp) {
         // ---------------- producers: queries once, then gathered row tiles.
-        // A tile is 16 row quads x 9 column blocks = 144 gather4 requests;
-        // producer thread pl sends requests pl and pl + 128.
+        // A tile is 16 row quads x 9 column blocks = 144 gather4 requests
+        // (8 blocks, 128 requests, without the rope tail); producer thread pl
+        // sends requests pl and pl + 128.
         const int pl = (int)threadIdx.x - 32 * (kMmaWarp + 1);
         if (pl == 0) {
             const uint32_t qf = smem_u32(&ctl.q_full);
-            mbar_arrive_expect_tx(qf, kQBytes);
+            mbar_arrive_expect_tx(qf, p.rope ? kQBytes : kQBytes - kQBlockBytes);
             const int32_t qrow = t * p.H;
             for (int kb = 0; kb < 8; ++kb)
                 tma_load_2d(smem_u32(q_s + kb * kQBlockBytes), &q_lat_map, qf, kb * 64, qrow);
-            tma_load_2d(smem_u32(q_s + 8 * kQBlockBytes), &q_rope_map, qf, 0, qrow);
+            if (p.rope) tma_load_2d(smem_u32(q_s + 8 * kQBlockBytes), &q_rope_map, qf, 0, qrow);
         }
+        const int nb = p.rope ? kBlocks : kBlocks - 1;   // column blocks gathered per row
+        const int n_req = (kRows / 4) * nb;                // gather4 requests per tile
         pdl_wait();                                  // the indices come from the preceding kernel
         // Rows of this thread's requests (at most two: 144 per tile, 128
         // producers) are looked up before the buffer is free, so the copies
@@ -219,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < kReq; ++u) {
                 const int q = pl + u * kProducers;
-                if (q >= (kRows / 4) * kBlocks) break;
-                const int quad = q / kBlocks, kb = q % kBlocks;
+                if (q >= n_req) break;
+                const int quad = p.rope ? q / kBlocks : q >> 3, kb = p.rope ? q % kBlocks : q & 7;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int e = (tile_lo + it) * kRows + quad * 4 + j;
@@ -242,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status)) break;
             const uint32_t full = smem_u32(&ctl.c_full[buf]);
-            if (pl == 0) mbar_arrive_expect_tx(full, kCBytes);
+            if (pl == 0) mbar_arrive_expect_tx(full, p.rope ? kCBytes : kCBytes - kCBlockBytes);
 #pragma unroll
             for (int u = 0; u < kReq; ++u) {
                 const int q = pl + u * kProducers;
-                if (q >= (kRows / 4) * kBlocks) break;
-                const int quad = q / kBlocks, kb = q % kBlocks;
+                if (q >= n_req) break;
+                const int quad = p.rope ? q / kBlocks : q >> 3, kb = p.rope ? q % kBlocks : q & 7;
                 tma_gather4(smem_u32(c_s + buf * kCBytes + kb * kCBlockBytes + quad * 512), &kv_map, full, kb * 64,
                             rr[u][0], rr[u][1], rr[u][2], rr[u][3]);
             }
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t cb = ca + buf * kCBytes;
 #pragma unroll 1
-                    for (int kb = 0; kb < kBlocks; ++kb) {
+                    for (int kb = 0; kb < (p.rope ? kBlocks : kBlocks - 1); ++kb) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             const uint64_t ad = sdesc_sw128(cb + kb * kCBlockBytes + ks * 32, 16, 1024);
@@ -567,6 +574,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     p.tiles_per_cta = a.tiles_per_cta;
     p.n_split = a.n_split;
     p.n_tiles = (a.k + kRows - 1) / kRows;
+    p.rope = a.rope;
     const size_t smem = sparse_attn_smem_bytes();
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(sparse_attn_kernel), 1, smem);
     if (e != cudaSuccess) return e;

@@ -198,6 +198,21 @@ dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope,
                                  cudaStream_t stream);
 
 /*
+ * MLA-NoPE sparse attention: vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on
+ * gfx1030", whose DSA layers cache the 512-d kv latent per token and apply no
+ * RoPE anywhere.  As dsa_sparse_mla_attn without the rope tail:
+ *   z_j      = sm_scale * q_lat[t,h] . c_j,   c_j = kv_latent[kv_off[b] + idx[t,j]]
+ *   out[t,h] = sum_j softmax(z)_j * c_j,  lse[t,h] = log(sum_j exp(z_j))
+ *   q_lat [T,H,512] bf16, kv_latent [cache_rows,512] bf16 (1024-byte rows)
+ * Everything else (idx, out, lse, workspace DSA_OP_SPARSE_ATTN, errors) as
+ * dsa_sparse_mla_attn.
+ */
+dsa_status_t dsa_sparse_mla_attn_nope(const dsa_bf16 *q_lat, const dsa_bf16 *kv_latent,
+                                      const dsa_batch_t *batch, const int32_t *idx, int k, int H,
+                                      float sm_scale, float *out, float *lse, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/*
  * The fused step ([IDX], [KC], [MLA]): append the new indexer keys, score
  * every query against its visible keys, select the top-k positions and
  * attend over them -- in that stream order, so each token's own key is in
