@@ -36,6 +36,18 @@ def test_exports_every_declared_symbol(L):
     assert set(declared()) == set(dsa.SIGNATURES), "binding and header disagree"
 
 
+def test_binding_signatures_match_the_header_arity():
+    """Every declaration's parameter count equals the binding's argtypes."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = re.findall(r"\b(?:dsa_status_t|int|const char\s*\*)\s*(dsa_[a-z0-9_]+)\s*\(([^;]*?)\)\s*;", src,
+                       flags=re.S)
+    assert {n for n, _ in decls} == set(dsa.SIGNATURES)
+    for name, params in decls:
+        p = params.strip()
+        n = 0 if p in ("", "void") else p.count(",") + 1
+        assert n == len(dsa.SIGNATURES[name][1]), name
+
+
 def test_device_status_bits_match_the_header():
     """The binding's DSA_DEV_* constants are the header's enum values."""
     src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
