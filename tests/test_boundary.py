@@ -87,6 +87,25 @@ def test_workspace_sizes(L):
     assert L.dsa_workspace_size(0, None, 32, 64, 16, C.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
 
 
+def test_decode_launch_counts(L):
+    """dsa_decode enqueues: an append unless every sequence has one token
+    (then the score kernel appends), a score and a top-k per score window
+    (1 GiB slab), the attention, and a combine when tokens are split."""
+    n = C.c_int()
+    cases = [
+        (dict(batch=8, total_q=8, max_q_per_seq=1, max_kv=8192, cache_rows=8 * 8192), 2048, 4),
+        (dict(batch=1, total_q=4096, max_q_per_seq=4096, max_kv=8192, cache_rows=8192), 2048, 4),
+        (dict(batch=1, total_q=16384, max_q_per_seq=16384, max_kv=131072, cache_rows=131072), 2048, 18),
+    ]
+    for kw, k, want in cases:
+        b = _batch(**kw)
+        assert L.dsa_decode_launches(C.byref(b), 32, 64, k, C.byref(n)) == dsa.DSA_OK
+        assert n.value == want, (kw, n.value)
+    assert L.dsa_decode_launches(C.byref(_batch()), 32, 64, 0, C.byref(n)) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_decode_launches(None, 32, 64, 16, C.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert L.dsa_decode_launches(C.byref(_batch()), 32, 64, 16, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+
+
 def test_argument_validation_runs_before_any_launch(L):
     b = _batch()
     ws, nws = C.c_void_p(0x10000), 1 << 20
