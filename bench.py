@@ -226,20 +226,64 @@ def gpu_index_for(device):
 
 # ---------------------------------------------------------------------------- oracle (CPU) legs
 
+def token_subs(wl, inp, tokens):
+    """Single-token workloads: token t of wl decoded alone over its own
+    sequence's keys 0..q_pos[t] (the same work it has in the full step)."""
+    import numpy as np
+    import dsa_synth as S
+    subs = []
+    for t in tokens:
+        b = int(np.searchsorted(wl.cu_q, t, side="right") - 1)
+        off, p = wl.kv_off[b], wl.q_pos[t]
+        one = S.Workload(wl.name, wl.seed, [p + 1], [p], [0, 1], wl.H_I, wl.H, wl.top_k, wl.hadamard, wl.sm_scale)
+        sl = slice(off, off + p + 1)
+        subs.append((one, S.Inputs(k_cache=inp.k_cache[sl], k_new=inp.k_new[t:t + 1], q_idx=inp.q_idx[t:t + 1],
+                                   w=inp.w[t:t + 1], q_lat=inp.q_lat[t:t + 1], q_rope=inp.q_rope[t:t + 1],
+                                   kv_cache=inp.kv_cache[sl])))
+    return subs
+
+
 def run_oracle_sample(wl, inp, seconds):
-    """Times the oracle's whole step on the full batch, repeated within the budget."""
+    """Times the oracle on the host cores within a budget: whole steps of a
+    decode batch, or, for a prefill chunk (whose full step would take
+    minutes to hours), up to 64 of its tokens spread evenly over the chunk,
+    each decoded alone over its full key range -- tokens per second
+    extrapolate to the chunk by token count.  Also the middle token of the
+    workload, decoded alone on a single thread."""
     import oracle
     cores = oracle.set_threads(0)
-    reps, t0 = 0, time.perf_counter()
+    if wl.T <= 64:
+        def one(i):
+            oracle.decode(inp, wl)
+            return wl.T
+        what = f"full steps of the {wl.name} workload ({wl.T} query tokens each)"
+    else:
+        subs = token_subs(wl, inp, range(0, wl.T, -(-wl.T // 64)))
+
+        def one(i):
+            o, si = subs[i % len(subs)]
+            oracle.decode(si, o)
+            return 1
+        what = (f"tokens of {wl.name} ({len(subs)} spread evenly over the {wl.T}-token chunk, each decoded "
+                f"alone over its full key range; extrapolated to the chunk by token count)")
+    reps, toks, t0 = 0, 0, time.perf_counter()
     while True:
-        oracle.decode(inp, wl)
+        toks += one(reps)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds or reps >= 50:
             break
-    return dict(value=wl.T * reps / el, unit=UNIT, cores=cores, kind="oracle",
-                sample=f"{reps} full steps of the {wl.name} workload ({wl.T} query tokens each), "
-                       f"{el:.1f} s of CPU time on {cores} OpenMP threads")
+    ((o1, s1),) = token_subs(wl, inp, [wl.T // 2])
+    oracle.set_threads(1)
+    t1 = time.perf_counter()
+    oracle.decode(s1, o1)
+    el1 = time.perf_counter() - t1
+    oracle.set_threads(0)
+    return dict(value=toks / el, unit=UNIT, cores=cores, kind="oracle",
+                sample=f"{reps} {what}, {el:.1f} s of CPU time on {cores} OpenMP threads",
+                single_thread={"value": 1.0 / el1, "unit": UNIT, "cores": 1,
+                               "sample": f"token {wl.T // 2} of {wl.name} decoded alone over its full key "
+                                         f"range on one thread, {el1:.2f} s"})
 
 
 def reference_arm(args):
@@ -248,21 +292,12 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import numpy as np
     import dsa_synth as S
     import oracle
     wl = S.config(WORKLOADS[args.workload])
     inp = S.make_inputs(wl)
     cores = oracle.set_threads(0)
-    subs = []
-    for t in range(wl.T if wl.T <= 64 else 64):
-        b = int(np.searchsorted(wl.cu_q, t, side="right") - 1)
-        off, p = wl.kv_off[b], wl.q_pos[t]
-        one = S.Workload(wl.name, wl.seed, [p + 1], [p], [0, 1], wl.H_I, wl.H, wl.top_k, wl.hadamard, wl.sm_scale)
-        sl = slice(off, off + p + 1)
-        subs.append((one, S.Inputs(k_cache=inp.k_cache[sl], k_new=inp.k_new[t:t + 1], q_idx=inp.q_idx[t:t + 1],
-                                   w=inp.w[t:t + 1], q_lat=inp.q_lat[t:t + 1], q_rope=inp.q_rope[t:t + 1],
-                                   kv_cache=inp.kv_cache[sl])))
+    subs = token_subs(wl, inp, range(min(wl.T, 64)))
     stack = args.workload == "indexshare_decode"
 
     def one_step(i):

@@ -27,3 +27,22 @@ def test_no_recorded_window_falls_back_to_the_first_top_k():
     t = [0.0, 1.0, 3.0, 4.0, 5.0]
     st = bench.stage_split(t, [])
     assert st["topk"] == pytest.approx(2.0) and st["indexer_score"] == pytest.approx(1.0)
+
+
+def test_cpu_baseline_is_bounded_and_reports_one_thread():
+    """Whole steps for a small decode batch; for a chunk of more than 64
+    tokens a spread sample of single-token decodes (a full prefill step of
+    the oracle would take minutes to hours); a single-thread figure."""
+    import dsa_synth as S
+    for wl in (S.config(1), S.prefill_workload("p", 3, 200, 130, H_I=4, H=8, top_k=64)):
+        inp = S.make_inputs(wl)
+        cb = bench.run_oracle_sample(wl, inp, 0.05)
+        assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+        assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+        if wl.T > 64:
+            assert "spread evenly" in cb["sample"]
+        else:
+            assert "full steps" in cb["sample"]
+    subs = bench.token_subs(wl, inp, [0, 129])
+    assert [o.q_pos for o, _ in subs] == [[200], [329]]
+    assert subs[1][1].k_cache.shape[0] == 330
