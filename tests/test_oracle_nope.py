@@ -13,6 +13,7 @@ the output is the softmax-weighted sum of the selected latent rows.
     gives zero and -inf.
 """
 import numpy as np
+import pytest
 
 import dsa_synth as S
 import oracle
@@ -76,3 +77,11 @@ def test_single_row_equal_scores_and_empty_rows():
         assert np.allclose(out[1, h], (C[3] + C[30]) / 2, rtol=0, atol=1e-12)
         assert abs(lse[1, h] - np.log(2.0)) < 1e-12
         assert np.all(out[2, h] == 0) and lse[2, h] == -np.inf
+
+
+def test_non_causal_index_is_rejected():
+    wl, inp = _case(L=50, H=2, pos=(20,))
+    idx = np.array([[3, 21, -1]], np.int32)        # 21 > q_pos = 20
+    latent = np.ascontiguousarray(inp.kv_cache[:, :512])
+    with pytest.raises(ValueError, match="code -2"):
+        oracle.sparse_attn_nope(inp.q_lat, latent, oracle.Batch.of(wl), idx, 0.1)
