@@ -117,12 +117,18 @@ def _stream(stream=None):
     return C.c_void_p(s.cuda_stream)
 
 
+# Fixed innermost extents of the tensors the calls take (include/dsa.h).
+_WIDTH = {"k_new": 128, "q_idx": 128, "k_cache": 128, "q_lat": 512, "q_rope": 64, "kv_cache": 576,
+          "kv_latent": 512, "out": 512}
+
+
 def _req(t, dtype, name):
-    import torch
     if t is None:
         return
     if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
         raise TypeError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} on {t.device}")
+    if name in _WIDTH and (t.dim() < 2 or t.shape[-1] != _WIDTH[name]):
+        raise TypeError(f"{name}: expected rows of {_WIDTH[name]} elements, got shape {tuple(t.shape)}")
 
 
 @dataclass

@@ -163,3 +163,33 @@ def test_product_path_never_touches_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(root, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_binding_rejects_rows_of_the_wrong_width():
+    """The binding checks each tensor's innermost extent before any call
+    (a 576-wide cache passed where 512-wide latent rows are expected would
+    otherwise be read with the wrong stride)."""
+    import torch
+
+    class Fake:                                # stands in for a CUDA tensor; no GPU needed
+        is_cuda = True
+        dtype = torch.bfloat16
+        device = "cuda:0"
+
+        def __init__(self, *shape):
+            self.shape = shape
+
+        def is_contiguous(self):
+            return True
+
+        def dim(self):
+            return len(self.shape)
+
+    dsa._req(Fake(100, 512), torch.bfloat16, "kv_latent")
+    with pytest.raises(TypeError, match="rows of 512"):
+        dsa._req(Fake(100, 576), torch.bfloat16, "kv_latent")
+    with pytest.raises(TypeError, match="rows of 576"):
+        dsa._req(Fake(100, 512), torch.bfloat16, "kv_cache")
+    with pytest.raises(TypeError, match="rows of 64"):
+        dsa._req(Fake(8, 64, 32), torch.bfloat16, "q_rope")
+    dsa._req(Fake(8, 64), torch.bfloat16, "w")                  # no fixed width
