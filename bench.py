@@ -3,16 +3,20 @@
 score, top-k, sparse MLA attention) on GB300.
 
 One step = one fused dsa_decode call over one batch of synthetic inputs
-already resident in HBM.  Default workload: batched decode, 8 sequences of
+already resident in HBM.  Headline workload: batched decode, 8 sequences of
 8192 cached positions, 32 indexer heads x 128, 64 query heads, top-2048,
-576-wide bf16 latent rows.  Each step is the library's own stream launches
-(--graph replays a CUDA graph of the step instead); L2 is flushed (a 512 MB
-write) before every timed step and each step is timed with CUDA events on
-its stream.  The library's trace events
-split every timed step into its kernels, which gives the per-kernel
-durations behind the roofline object.
+576-wide bf16 latent rows.  The same default run then measures the rest of
+the metric the same way under "workloads": the ragged long-context decode
+(32 sequences of 4k-64k positions, rotation on) and the two prefill
+workloads (4096 tokens after 4096, 16384 after 114688).  Each step is the
+library's own stream launches (--graph replays a CUDA graph of the step
+instead); L2 is flushed (a 512 MB write, then a 512 MB read) before every
+timed step and each step is timed with CUDA events on its stream.  Each
+kernel's time inside the overlapped step comes from the library's device
+timeline (globaltimer at the first CTA start and last CTA end of every
+kernel), which gives the per-kernel rooflines.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--headline-only]
   python bench.py --impl reference ...    # the CPU oracle on the same workload
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
@@ -67,6 +71,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="measure only the chosen workload (by default the batched-decode run also measures the "
+                         "ragged decode and the two prefill workloads)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each step as a CUDA graph (default: the library's own stream launches, which "
                          "measured 2.8 us faster per batched-decode step on GB300: a graph replay adds "
@@ -102,7 +109,8 @@ def algorithmic(wl):
     attn_bytes = sel * 1152
     return dict(score_bytes=score_bytes, score_flops=pairs * wl.H_I * 256,
                 attn_bytes=attn_bytes, attn_flops=sel * wl.H * 2 * (576 + 512),
-                step_bytes=score_bytes + attn_bytes)
+                step_bytes=score_bytes + attn_bytes,
+                topk_bytes=pairs * 4, append_bytes=wl.T * (512 + 256), out_bytes=wl.T * wl.H * 512 * 4)
 
 
 def source_hash(kernel):
@@ -504,36 +512,57 @@ def layer_stack(args):
 
 # ---------------------------------------------------------------------------- GPU arm
 
-def main():
-    args = parse()
-    if args.impl == "reference":
-        return reference_arm(args)
-    if args.workload == "indexshare_decode":
-        return layer_stack(args)
+TIMELINE_ORDER = ["k_append", "indexer_score", "topk", "sparse_attn", "attn_combine"]
+EXTRA_WORKLOADS = ["ragged_decode", "prefill_chunk", "long_prefill"]
 
+
+def exclusive_spans(spans):
+    """Per-kernel time inside one overlapped step, from the device timeline.
+
+    spans: stage -> (first CTA start, last CTA end) in us.  A kernel launched
+    with programmatic dependent launch starts its prologue while its
+    predecessor still runs and then waits for it, so its own share of the
+    step runs from the later of its first CTA start and the predecessor's last
+    CTA end, to its own last CTA end.  The shares add up to the step's span.
+    """
+    out, prev_end = {}, None
+    for st in TIMELINE_ORDER:
+        if st not in spans:
+            continue
+        a, b = spans[st]
+        lo = a if prev_end is None else max(a, prev_end)
+        out[st] = max(0.0, b - lo)
+        prev_end = b
+    return out
+
+
+def kernel_roofline(stage, ms, wl, alg, pk):
+    """Roofline of one kernel over one step: decode contractions stream HBM
+    (bytes they must read), prefill contractions run on the tensor cores
+    (causal flops of the definition; fp16 and bf16 share one dense peak), the
+    selection reads its score rows once, the combine writes the outputs."""
+    decode = wl.max_q_per_seq == 1
+    sec = ms * 1e-3
+    if stage in ("indexer_score", "sparse_attn") and not decode:
+        flops = alg["score_flops"] if stage == "indexer_score" else alg["attn_flops"]
+        ach = flops / sec / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"], "frac_of_sustained": ach / pk["bf16_tflops_sustained"],
+                "dtype": "fp16" if stage == "indexer_score" else "bf16", "algorithmic_flops": flops}
+    nbytes = {"indexer_score": alg["score_bytes"], "sparse_attn": alg["attn_bytes"], "topk": alg["topk_bytes"],
+              "k_append": alg["append_bytes"], "attn_combine": alg["out_bytes"]}[stage]
+    ach = nbytes / sec / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+            "algorithmic_bytes": nbytes}
+
+
+def measure(dsa, torch, wl, steps, warmup, flush_mb, world=1, e2e_steps=0, graph=False):
+    """Times one workload: `steps` steps (each on a cold L2, CUDA events on
+    the launching stream), then per-kernel times from the device timeline of
+    up to 200 more steps, and from the stage events.  Returns the measured
+    numbers and, with e2e_steps, the end-to-end rate through the binding."""
     import numpy as np
-    import torch
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.cuda.current_device()
-
-    from dsa_sparse_attention_score_gb300 import build as lib_build
-    if rank == 0 or world == 1:
-        lib_build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    import dsa_sparse_attention_score_gb300 as dsa
     import dsa_synth as S
-
-    wl = S.config(WORKLOADS[args.workload])
     inp = S.make_inputs(wl)
 
     def up(a):
@@ -556,17 +585,18 @@ def main():
     k_new, q_idx, w, q_lat, q_rope = [d_pack[off:off + a.nbytes].view(dt).view(a.shape)
                                       for (a, dt), off in zip(step_in, offs)]
     k_cache, kv_cache = up(inp.k_cache), up(inp.kv_cache)
+    del inp
     batch = dsa.Batch.from_host(wl.cu_q, wl.q_pos, wl.kv_off, wl.cache_rows, max_q_per_seq=wl.max_q_per_seq,
                                 max_kv=wl.max_kv)
     ws = dsa.workspace(dsa.DSA_OP_DECODE, batch, wl.H_I, wl.H, wl.top_k)
     out = torch.empty((wl.T, wl.H, 512), device="cuda")
     lse = torch.empty((wl.T, wl.H), device="cuda")
     idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device="cuda")
-    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(flush_mb << 20, dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones((flush_mb << 20) // 4, dtype=torch.float32, device="cuda")
     launches = dsa.dsa_decode_launches(batch, wl.H_I, wl.H, wl.top_k)
-
     trace = [torch.cuda.Event(enable_timing=True) for _ in range(6 + 2 * MAX_TRACE_WINDOWS)]
-    flush_r = torch.ones((args.flush_mb << 20) // 4, dtype=torch.float32, device="cuda")
+    tl_buf = torch.zeros(10, dtype=torch.int64, device="cuda")
 
     def flush_l2(i):
         # write a buffer larger than L2, then read another one, so the step
@@ -581,156 +611,208 @@ def main():
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    graph = graph_traced = None
-    if args.graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
+    run = step
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
             step()
-        dsa.dsa_set_trace_events(trace)
-        graph_traced = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_traced):
-            step()
-        dsa.dsa_set_trace_events(None)
-        torch.cuda.synchronize()
-    run = graph.replay if graph is not None else step
-    # a third capture with the device timeline on: real start/end of each
-    # kernel inside an overlapped step (the timeline buffer is baked in)
-    tl_buf = torch.zeros(10, dtype=torch.int64, device="cuda")
-    graph_tl = None
-    if graph is not None:
-        dsa.dsa_set_timeline(tl_buf)
-        graph_tl = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_tl):
-            step()
-        dsa.dsa_set_timeline(None)
-        torch.cuda.synchronize()
-
-    def run_traced():
-        if graph_traced is not None:
-            graph_traced.replay()
-        else:
-            dsa.dsa_set_trace_events(trace)
-            step()
-            dsa.dsa_set_trace_events(None)
-
-    def run_timeline():
-        if graph_tl is not None:
-            graph_tl.replay()
-        else:
-            dsa.dsa_set_timeline(tl_buf)
-            step()
-            dsa.dsa_set_timeline(None)
-
-    for i in range(args.warmup):
+        run = g.replay
+    for i in range(warmup):
         flush_l2(i)
         run()
-        run_traced()
     torch.cuda.synchronize()
     if dsa.dsa_read_device_status(ws) != 0:
-        raise RuntimeError("device status flags set during warm-up")
+        raise RuntimeError(f"{wl.name}: device status flags set during warm-up")
 
     # ---- timed region: K steps, each on a cold L2, timed on the device
-    clocks = Clocks(gpu_index_for(dev))
+    clocks = Clocks(gpu_index_for(torch.cuda.current_device()))
     time.sleep(0.2)                                  # let the sampler start
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
         flush_l2(i)
         ev[i][0].record()
         run()
         ev[i][1].record()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_rows = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    # the same step with stage events (they serialise the stages): per-kernel time
-    stage_ms = {s: [] for s in STAGES}
-    for i in range(min(args.steps, 200)):
+
+    # ---- per-kernel times: the device timeline of the same step (earliest
+    # CTA start / latest CTA end of each kernel), and stage events (which
+    # serialise the kernels; used where score and top-k run in several windows)
+    n_side = min(steps, 200)
+    big = torch.iinfo(torch.int64).max
+    excl = {st: [] for st in TIMELINE_ORDER}
+    spans = {st: [] for st in TIMELINE_ORDER}
+    for i in range(n_side):
+        tl_buf[0::2] = big
+        tl_buf[1::2] = 0
         flush_l2(i)
-        run_traced()
+        dsa.dsa_set_timeline(tl_buf)
+        step()
+        dsa.dsa_set_timeline(None)
+        torch.cuda.synchronize()
+        v = tl_buf.tolist()
+        t0 = min(x for x in v[0::2] if x != big)
+        sp = {st: ((v[2 * j] - t0) / 1e3, (v[2 * j + 1] - t0) / 1e3)
+              for j, st in enumerate(TIMELINE_ORDER) if v[2 * j] != big}
+        for st, x in sp.items():
+            spans[st].append(x)
+        for st, x in exclusive_spans(sp).items():
+            excl[st].append(x)
+    stage_ms = {st: [] for st in STAGES}
+    for i in range(n_side):
+        flush_l2(i)
+        dsa.dsa_set_trace_events(trace)
+        step()
+        dsa.dsa_set_trace_events(None)
         trace[5].synchronize()
         t = [trace[0].elapsed_time(trace[j]) for j in range(1, 6)]
         pairs = [(trace[0].elapsed_time(trace[6 + 2 * j]), trace[0].elapsed_time(trace[7 + 2 * j]))
                  for j in range(MAX_TRACE_WINDOWS)]
-        for s_, v in stage_split(t, pairs).items():
-            stage_ms[s_].append(v)
-    # the step with the device timeline: per-kernel [start, end] inside a step
-    tl = {s: [] for s in STAGES}
-    big = torch.iinfo(torch.int64).max
-    for i in range(min(args.steps, 200)):
-        tl_buf[0::2] = big
-        tl_buf[1::2] = 0
-        flush_l2(i)
-        run_timeline()
-        torch.cuda.synchronize()
-        v = tl_buf.tolist()
-        t0 = min(x for x in v[0::2] if x != big)
-        for j, s_ in enumerate(STAGES):
-            if v[2 * j] != big:
-                tl[s_].append(((v[2 * j] - t0) / 1e3, (v[2 * j + 1] - t0) / 1e3))
+        for st, x in stage_split(t, pairs).items():
+            stage_ms[st].append(x)
     torch.cuda.synchronize()
+    windows = score_windows(dsa, batch)
+    if windows == 1:
+        kernel_ms = {st: statistics.median(v) / 1e3 for st, v in excl.items() if v}
+        source = ("device timeline (globaltimer): each kernel's exclusive span in the overlapped step, from the "
+                  "later of its first CTA start and its predecessor's last CTA end to its last CTA end; "
+                  f"median of {n_side} steps")
+    else:
+        kernel_ms = {st: statistics.median(v) for st, v in stage_ms.items() if v and statistics.median(v) > 0}
+        source = (f"stage events around each of the {windows} score windows' top-k launches (the score and "
+                  f"top-k kernels alternate, so their timeline spans overlap); median of {n_side} steps")
+
+    res = dict(step_ms=step_ms, kernel_ms=kernel_ms, kernel_source=source, launches=launches,
+               clocks=Clocks.summary(clock_rows),
+               timeline_us={st: [round(statistics.median(a for a, _ in v), 2),
+                                 round(statistics.median(b for _, b in v), 2)] for st, v in spans.items() if v},
+               stages_ms={st: round(statistics.median(v), 5) for st, v in stage_ms.items() if v})
+
+    if e2e_steps:
+        # ---- end to end through the public API with host buffers
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_ms = []
+        for i in range(e2e_steps + 3):
+            flush_l2(i)
+            e0.record()
+            d_pack.copy_(h_pack, non_blocking=True)   # every input of the step, one copy
+            step()
+            h_out.copy_(out, non_blocking=True)
+            e1.record()
+            e1.synchronize()
+            if i >= 3:
+                e2e_ms.append(e0.elapsed_time(e1))
+        res["e2e_ms"] = e2e_ms
+        res["h2d"] = h_pack.numel()
+        res["d2h"] = h_out.numel() * h_out.element_size()
+    if dsa.dsa_read_device_status(ws) != 0:
+        raise RuntimeError(f"{wl.name}: device status flags set during the timed steps")
+    return res
+
+
+def score_windows(dsa, batch):
+    """Score windows of one dsa_decode call (query tokens are scored in
+    windows whose scores fit the workspace's 1 GiB slab).  The call launches
+    an append (unless every sequence has one token), a score and a top-k per
+    window, the attention, and a combine when tokens are split; with k = 1
+    no token is split."""
+    n = dsa.dsa_decode_launches(batch, 1, 64, 1)
+    append = 0 if batch.max_q_per_seq == 1 else 1
+    return (n - append - 1) // 2
+
+
+def workload_line(wl, res, pk, steps, headline=False):
+    """The numbers of one workload: throughput, per-kernel rooflines, the
+    dominant kernel (longest per-kernel time) and the whole step against the
+    HBM roofline of the bytes it must move."""
+    alg = algorithmic(wl)
+    ms = statistics.fmean(res["step_ms"])
+    kernels = {st: dict(ms=round(m, 5), **kernel_roofline(st, m, wl, alg, pk)) for st, m in res["kernel_ms"].items()}
+    dom = max(res["kernel_ms"], key=res["kernel_ms"].get)
+    roof = dict(kernels[dom])
+    roof["kernel"] = KERNEL_OF_STAGE[dom]
+    roof["ms_per_launch_note"] = res["kernel_source"]
+    roof["peak_source"] = f"{pk['source']} (MEASURED_PEAKS.json)" if pk["source"] == "measured" else "fallback"
+    roof["traffic"] = ncu_traffic(KERNEL_OF_STAGE[dom], wl.name)
+    step_gbs = alg["step_bytes"] / (ms * 1e-3) / 1e9
+    line = {"workload": wl.name, "kind": "decode" if wl.max_q_per_seq == 1 else "prefill", "B": wl.B, "T": wl.T,
+            "L": wl.max_kv, "H_I": wl.H_I, "H": wl.H, "top_k": wl.top_k, "hadamard": wl.hadamard,
+            "steps": steps, "ms_per_step": ms, "tok_s": wl.T / (ms * 1e-3),
+            "roofline": roof, "kernels": kernels,
+            "step_roofline": {"bound": "hbm", "algorithmic_bytes": alg["step_bytes"], "achieved": step_gbs,
+                              "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": step_gbs / pk["hbm_gbs"]},
+            "timeline_us": res["timeline_us"], "stages_ms": res["stages_ms"], "clocks": res["clocks"],
+            "gpu_launches_per_step": res["launches"]}
+    return line
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    if args.workload == "indexshare_decode":
+        return layer_stack(args)
+
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+
+    from dsa_sparse_attention_score_gb300 import build as lib_build
+    if rank == 0 or world == 1:
+        lib_build.build()
     if world > 1:
         torch.distributed.barrier()
-    clock_rows = clocks.stop()
+    import dsa_sparse_attention_score_gb300 as dsa
+    import dsa_synth as S
 
-    total_s = max_over_ranks(sum(step_ms) / 1e3)
+    pk = peaks()
+    wl = S.config(WORKLOADS[args.workload])
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    res = measure(dsa, torch, wl, args.steps, args.warmup, args.flush_mb, world=world, e2e_steps=n_e2e,
+                  graph=args.graph)
+    total_s = max_over_ranks(sum(res["step_ms"]) / 1e3)
     ms_per_step = 1e3 * total_s / args.steps
     value = job_throughput(world, wl.T, args.steps, total_s)
-
-    # ---- end to end through the public API with host buffers
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = h_pack.numel()
-    d2h = h_out.numel() * h_out.element_size()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_e2e = max(1, min(args.e2e_steps, args.steps))
-    e2e_ms = []
-    for i in range(n_e2e + 3):
-        flush_l2(i)
-        e0.record()
-        d_pack.copy_(h_pack, non_blocking=True)   # every input of the step, one copy
-        step()
-        h_out.copy_(out, non_blocking=True)
-        e1.record()
-        e1.synchronize()
-        if i >= 3:
-            e2e_ms.append(e0.elapsed_time(e1))
-    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3)
+    e2e_s = max_over_ranks(sum(res["e2e_ms"]) / 1e3)
     e2e_value = job_throughput(world, wl.T, n_e2e, e2e_s)
-    if dsa.dsa_read_device_status(ws) != 0:
-        raise RuntimeError("device status flags set during the timed steps")
+    head = workload_line(wl, res, pk, args.steps, headline=True)
+    gpu_launches = res["launches"] * args.steps
 
+    # ---- the rest of the metric: the ragged long-context decode and the two
+    # prefill workloads, each on its own (fewer steps for the long ones)
+    extra = {}
+    if not args.headline_only and args.workload == "batched_decode":
+        for name in EXTRA_WORKLOADS:
+            torch.cuda.empty_cache()
+            w2 = S.config(WORKLOADS[name])
+            n2 = max(3, min(args.steps, 20 if name != "long_prefill" else 10))
+            r2 = measure(dsa, torch, w2, n2, max(3, min(args.warmup, 5)), args.flush_mb, world=world)
+            extra[name] = workload_line(w2, r2, pk, n2)
+            extra[name]["ms_per_step"] = 1e3 * max_over_ranks(sum(r2["step_ms"]) / 1e3) / n2
+            extra[name]["tok_s"] = job_throughput(world, w2.T, n2, 1e-3 * extra[name]["ms_per_step"] * n2)
+            gpu_launches += r2["launches"] * n2
+            del r2
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
 
-    # ---- roofline of the dominant kernel
-    pk = peaks()
-    alg = algorithmic(wl)
-    mean = {s: statistics.fmean(v) for s, v in stage_ms.items()}
-    timeline = {s: [round(statistics.median(a for a, _ in v), 2), round(statistics.median(b for _, b in v), 2)]
-                for s, v in tl.items() if v}
-    dom = max(mean, key=mean.get)
-    decode = wl.max_q_per_seq == 1
-    if dom == "indexer_score" and not decode:
-        achieved = alg["score_flops"] / (mean[dom] * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "dtype": "fp16", "algorithmic_flops_per_launch": alg["score_flops"]}
-    elif dom in ("indexer_score", "sparse_attn"):
-        nbytes = alg["score_bytes"] if dom == "indexer_score" else alg["attn_bytes"]
-        achieved = nbytes / (mean[dom] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "algorithmic_bytes_per_launch": nbytes}
-    else:
-        roof = {"bound": "latency", "achieved": None, "peak": None, "unit": None}
-    if roof.get("achieved") is not None:
-        roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = KERNEL_OF_STAGE[dom]
-    roof["ms_per_launch"] = mean[dom]
-    roof["peak_source"] = f"{pk['source']} (MEASURED_PEAKS.json)" if pk["source"] == "measured" else "fallback"
-    roof["traffic"] = ncu_traffic(KERNEL_OF_STAGE[dom], wl.name)
-
-    step_gbs = alg["step_bytes"] / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -739,25 +821,31 @@ def main():
                    "top_k": wl.top_k, "hadamard": wl.hadamard,
                    "l2": f"flushed before every timed step ({args.flush_mb} MB write, then {args.flush_mb} MB "
                          "read of another buffer)",
-                   "launch": "CUDA graph replay" if graph is not None else
+                   "launch": "CUDA graph replay" if args.graph else
                              "stream launches through the C ABI (programmatic dependent launch between kernels)",
                    "parallelism": f"replicas x{world}"},
-        "clocks": Clocks.summary(clock_rows),
-        "gpu_launches": launches * args.steps,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        "clocks": res["clocks"],
+        "gpu_launches": gpu_launches,
+        "gpu_launches_note": "library kernels inside every timed step of the headline and of the workloads below",
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "steps": n_e2e, "path": "one pinned H2D copy of the step's packed inputs, dsa_decode through the Python "
                                         "binding, D2H of the output; caches stay resident"},
-        "roofline": roof,
-        "step_roofline": {"bound": "hbm", "algorithmic_bytes": alg["step_bytes"], "achieved": step_gbs,
-                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": step_gbs / pk["hbm_gbs"]},
-        "stages_ms": {s: round(m, 5) for s, m in mean.items()},
-        "stages_note": "per-kernel times from a second graph with stage events, which serialise the "
-                       "kernels that the headline graph overlaps (programmatic dependent launch)",
-        "timeline_us": timeline,
-        "timeline_note": "median [first CTA start, last CTA end] of each kernel inside an overlapped step, "
-                         "from the library's device timeline (globaltimer), relative to the first start",
+        "roofline": head["roofline"],
+        "kernels": head["kernels"],
+        "step_roofline": head["step_roofline"],
+        "timeline_us": head["timeline_us"],
+        "timeline_note": "median [first CTA start, last CTA end] of each kernel inside an overlapped step, from the "
+                         "library's device timeline (globaltimer), relative to the first start",
+        "stages_ms": head["stages_ms"],
+        "stages_note": "per-stage times with events between the stages (they serialise the kernels and add launch "
+                       "latency); the roofline uses the device timeline instead",
     }
+    if extra:
+        line["workloads"] = extra
+        line["workloads_note"] = ("the other workloads of the metric, each measured like the headline (cold L2, "
+                                  "CUDA events per step); prefill tok/s = query tokens of the chunk / step time")
     if world == 1 and not args.no_cpu_baseline:
+        inp = S.make_inputs(wl)
         line["cpu_baseline"] = run_oracle_sample(wl, inp, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     return 0

@@ -75,6 +75,7 @@ SIGNATURES = {
     "dsa_status_string": (C.c_char_p, [_I]),
     "dsa_set_trace_events": (_I, [_P, _I]),
     "dsa_set_timeline": (_I, [_P]),
+    "dsa_set_test_faults": (_I, [C.c_uint64, _I]),
     "dsa_version": (_I, []),
 }
 
@@ -396,6 +397,13 @@ _TRACE_KEEP = None
 def dsa_set_timeline(buf):
     """buf: CUDA int64/uint64 tensor of 10 slots, or None to disable."""
     _check(lib().dsa_set_timeline(_ptr(buf)), "dsa_set_timeline")
+
+
+def dsa_set_test_faults(wait_limit_ns: int = 0, skip_copies: bool = False):
+    """Failure-path test hook: bound every device wait by wait_limit_ns (0:
+    the default second) and, with skip_copies, make the score and attention
+    producers issue no copies so that the waits run out (DSA_DEV_TIMEOUT)."""
+    _check(lib().dsa_set_test_faults(int(wait_limit_ns), int(bool(skip_copies))), "dsa_set_test_faults")
 
 
 def dsa_status_string(code: int) -> str:

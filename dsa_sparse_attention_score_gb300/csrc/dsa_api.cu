@@ -11,13 +11,18 @@ using namespace dsa;
 
 namespace {
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0
 constexpr size_t kAlign = 256;
 constexpr int64_t kSlabBytes = int64_t(1) << 30;  // score slab budget in the workspace
 
 cudaEvent_t *g_trace = nullptr;
 int g_trace_n = 0;
 unsigned long long *g_timeline = nullptr;
+uint64_t g_wait_ns = kWaitLimitNs;    // failure-path test hooks (dsa_set_test_faults)
+int g_skip_copies = 0;
+
+constexpr int kMaxHeads = 128;        // query heads: one or two groups of 64 per token
+constexpr int kMaxSplit = 128;        // split partials the combine kernel merges
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -47,6 +52,8 @@ DevBatch dev_batch(const dsa_batch_t *b) {
     d.block_table = nullptr;
     d.max_blocks = 0;
     d.block_size = 0;
+    d.wait_ns = g_wait_ns;
+    d.skip_copies = g_skip_copies;
     return d;
 }
 
@@ -97,20 +104,25 @@ struct Layout {
     int n_split = 1, tiles_per_cta = 1;
 };
 
-// Splits of a token's selected rows across CTAs: with fewer tokens than SMs,
-// up to one wave of CTAs (one per SM), each keeping at least two tiles so
-// that its gathers overlap its arithmetic.
-void attn_split(int T, int k, int *n_split, int *tpc) {
+inline int head_groups(int H) { return (H + 63) / 64; }
+
+// Splits of a token's selected rows across CTAs: with fewer (token, head
+// group) pairs than SMs, up to one wave of CTAs (one per SM), each keeping at
+// least two tiles so that its gathers overlap its arithmetic, and never more
+// splits than the combine kernel merges.
+void attn_split(int T, int H, int k, int *n_split, int *tpc) {
     const int n_tiles = (k + attn_tile_rows() - 1) / attn_tile_rows();
+    const int64_t units = (int64_t)T * head_groups(H);
     int ns = 1;
-    if (T < kSMs) ns = std::max(1, std::min(n_tiles / 2, kSMs / T));
+    if (units < kSMs) ns = std::max(1, std::min(n_tiles / 2, (int)(kSMs / units)));
+    ns = std::min(ns, kMaxSplit);
     int t = (n_tiles + ns - 1) / ns;
     ns = (n_tiles + t - 1) / t;
     *n_split = ns;
     *tpc = t;
 }
 
-Layout layout(int op, const dsa_batch_t *b, int k) {
+Layout layout(int op, const dsa_batch_t *b, int H, int k) {
     Layout L;
     size_t off = kStatusBytes;
     if (op == DSA_OP_DECODE) {
@@ -126,13 +138,14 @@ Layout layout(int op, const dsa_batch_t *b, int k) {
         off = align_up(off + L.idx_bytes, kAlign);
     }
     if (op == DSA_OP_DECODE || op == DSA_OP_SPARSE_ATTN) {
-        attn_split(b->total_q, k, &L.n_split, &L.tiles_per_cta);
+        attn_split(b->total_q, H, k, &L.n_split, &L.tiles_per_cta);
         if (L.n_split > 1) {
+            const size_t rows = (size_t)b->total_q * L.n_split * head_groups(H) * 64;
             L.part_o = off;
-            L.part_o_bytes = (size_t)b->total_q * L.n_split * 64 * D_L * 4;
+            L.part_o_bytes = rows * D_L * 4;
             off = align_up(off + L.part_o_bytes, kAlign);
             L.part_ml = off;
-            L.part_ml_bytes = (size_t)b->total_q * L.n_split * 64 * 2 * 4;
+            L.part_ml_bytes = rows * 2 * 4;
             off = align_up(off + L.part_ml_bytes, kAlign);
         }
     }
@@ -249,26 +262,31 @@ dsa_status_t dsa_set_timeline(void *dev_buf) {
     return DSA_OK;
 }
 
+dsa_status_t dsa_set_test_faults(uint64_t wait_limit_ns, int skip_copies) {
+    g_wait_ns = wait_limit_ns ? wait_limit_ns : kWaitLimitNs;
+    g_skip_copies = skip_copies ? 1 : 0;
+    return DSA_OK;
+}
+
 dsa_status_t dsa_workspace_size(int op, const dsa_batch_t *batch, int H_I, int H, int k, size_t *bytes) {
     (void)H_I;
-    (void)H;
     if (!bytes || op < DSA_OP_K_APPEND || op > DSA_OP_DECODE) return DSA_ERR_INVALID_ARGUMENT;
     if (!batch || batch->batch < 1 || batch->total_q < 1 || batch->max_q_per_seq < 1 || batch->max_kv < 1)
         return DSA_ERR_INVALID_ARGUMENT;
     if ((op == DSA_OP_TOPK || op == DSA_OP_SPARSE_ATTN || op == DSA_OP_DECODE) && (k < 1 || k > 65536))
         return DSA_ERR_UNSUPPORTED;
-    *bytes = layout(op, batch, k).total;
+    if ((op == DSA_OP_SPARSE_ATTN || op == DSA_OP_DECODE) && (H < 1 || H > kMaxHeads)) return DSA_ERR_UNSUPPORTED;
+    *bytes = layout(op, batch, H, k).total;
     return DSA_OK;
 }
 
 dsa_status_t dsa_decode_launches(const dsa_batch_t *batch, int H_I, int H, int k, int *launches) {
     (void)H_I;
-    (void)H;
     if (!launches || !batch || batch->batch < 1 || batch->total_q < 1 || batch->max_q_per_seq < 1 ||
         batch->max_kv < 1)
         return DSA_ERR_INVALID_ARGUMENT;
-    if (k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
-    const Layout L = layout(DSA_OP_DECODE, batch, k);
+    if (k < 1 || k > 65536 || H < 1 || H > kMaxHeads) return DSA_ERR_UNSUPPORTED;
+    const Layout L = layout(DSA_OP_DECODE, batch, H, k);
     const int slabs = (batch->max_q_per_seq + L.J - 1) / L.J;
     const bool combine = L.n_split > 1;
     *launches = (batch->max_q_per_seq == 1 ? 0 : 1) + 2 * slabs + 1 + (combine ? 1 : 0);
@@ -368,12 +386,12 @@ dsa_status_t dsa_sparse_mla_attn_nope(const dsa_bf16 *q_lat, const dsa_bf16 *kv_
     dsa_status_t s = check_batch(batch);
     if (s != DSA_OK) return s;
     if (!q_lat || !kv_latent || !idx || !out) return DSA_ERR_INVALID_ARGUMENT;
-    if (H < 1 || H > 64 || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    if (H < 1 || H > kMaxHeads || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
     if ((int64_t)batch->total_q * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
     if (!aligned(q_lat, 16) || !aligned(kv_latent, 16) || !aligned(out, 16) || !aligned(idx, 4) ||
         (lse && !aligned(lse, 4)))
         return DSA_ERR_MISALIGNED;
-    const Layout L = layout(DSA_OP_SPARSE_ATTN, batch, k);
+    const Layout L = layout(DSA_OP_SPARSE_ATTN, batch, H, k);
     if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
     return run_attention(q_lat, nullptr, kv_latent, batch, idx, k, H, sm_scale, out, lse, ws, L, stream,
                          false, false, nullptr, false);
@@ -386,12 +404,12 @@ dsa_status_t dsa_sparse_mla_attn(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, 
     dsa_status_t s = check_batch(batch);
     if (s != DSA_OK) return s;
     if (!q_lat || !q_rope || !kv_cache || !idx || !out) return DSA_ERR_INVALID_ARGUMENT;
-    if (H < 1 || H > 64 || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    if (H < 1 || H > kMaxHeads || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
     if ((int64_t)batch->total_q * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
     if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
         !aligned(idx, 4) || (lse && !aligned(lse, 4)))
         return DSA_ERR_MISALIGNED;
-    const Layout L = layout(DSA_OP_SPARSE_ATTN, batch, k);
+    const Layout L = layout(DSA_OP_SPARSE_ATTN, batch, H, k);
     if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
     return run_attention(q_lat, q_rope, kv_cache, batch, idx, k, H, sm_scale, out, lse, ws, L, stream,
                          false, false);
@@ -416,13 +434,13 @@ static dsa_status_t decode_impl(const void *k_new, int k_dtype, const dsa_f16 *q
     if (!k_new || !q_idx || !w || !q_lat || !q_rope || !k_cache || !kv_cache || !out)
         return DSA_ERR_INVALID_ARGUMENT;
     if (k_dtype != DSA_KEY_F32 && k_dtype != DSA_KEY_F16) return DSA_ERR_INVALID_ARGUMENT;
-    if (H_I < 1 || H_I > 64 || H < 1 || H > 64 || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
+    if (H_I < 1 || H_I > 64 || H < 1 || H > kMaxHeads || k < 1 || k > 65536) return DSA_ERR_UNSUPPORTED;
     if ((int64_t)batch->total_q * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
     if (!aligned(k_new, 16) || !aligned(q_idx, 16) || !aligned(w, 4) || !aligned(q_lat, 16) ||
         !aligned(q_rope, 16) || !aligned(k_cache, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
         (lse && !aligned(lse, 4)) || (idx_out && !aligned(idx_out, 4)))
         return DSA_ERR_MISALIGNED;
-    const Layout L = layout(DSA_OP_DECODE, batch, k);
+    const Layout L = layout(DSA_OP_DECODE, batch, H, k);
     if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
 
     DevBatch db = dev_batch(batch);

@@ -66,8 +66,9 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Every wait inside a CTA is bounded by this; a wait that runs out sets
-// DSA_DEV_TIMEOUT and makes the CTA wind down.
+// Every wait inside a CTA is bounded, by default by this; a wait that runs
+// out sets DSA_DEV_TIMEOUT and makes the CTA wind down.  The limit reaches
+// the kernels at run time (DevBatch::wait_ns), so that a test can shorten it.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Tracing: earliest start / latest end of a kernel's CTAs (globaltimer ns).
@@ -120,13 +121,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity to complete: false once
+// limit_ns nanoseconds have passed without it.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 

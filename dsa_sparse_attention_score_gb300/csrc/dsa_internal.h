@@ -45,6 +45,11 @@ struct DevBatch {
     // block_table[seq * max_blocks + pos / block_size] * block_size + pos % block_size.
     const int32_t *block_table;     // null: contiguous, row kv_off[seq] + pos
     int max_blocks, block_size;
+    // Failure-path test hooks (dsa_set_test_faults): the limit of every
+    // bounded wait, and whether the producers of the score and attention
+    // kernels skip their copies so that the consumers' waits run out.
+    uint64_t wait_ns;
+    int skip_copies;
 };
 
 // Cache row of position pos (0 <= pos < max_kv) of sequence seq, whose

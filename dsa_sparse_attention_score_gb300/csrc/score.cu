@@ -94,9 +94,9 @@ struct Smem {
 static_assert(512 * 256 + 3 * kTileBytes + sizeof(Smem) <= kSmemLimit, "score ring does not fit");
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Smem &sm,
-                                         uint32_t *status) {
+                                         uint32_t *status, uint64_t limit_ns) {
     if (*(volatile int32_t *)&sm.abort_flag) return false;
-    if (mbar_wait(bar, parity)) return true;
+    if (mbar_wait(bar, parity, limit_ns)) return true;
     *(volatile int32_t *)&sm.abort_flag = 1;
     flag(status, DSA_DEV_TIMEOUT);
     return false;
@@ -326,13 +326,14 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
-        // ---------------- TMA producer
-        if (lane == 0) {
+        // ---------------- TMA producer (issues nothing under the failure-path
+        // test hook, so that the MMA issuer's first wait runs out)
+        if (lane == 0 && !b.skip_copies) {
             for (int i = 0; i < n_mma; ++i) {
                 const int s = i % n_stages;
                 const uint32_t k = (uint32_t)(i / n_stages);
                 if (i == first_dependent) pdl_wait();
-                if (!wait_bar(smem_u32(&sm.empty[s]), (k & 1) ^ 1, sm, p.status)) break;
+                if (!wait_bar(smem_u32(&sm.empty[s]), (k & 1) ^ 1, sm, p.status, b.wait_ns)) break;
                 const uint32_t full = smem_u32(&sm.full[s]);
                 mbar_arrive_expect_tx(full, kTileBytes);
                 const uint32_t dst = smem_u32(stages + s * kTileBytes);
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
-        if (lane == 0 && wait_bar(smem_u32(&sm.q_ready), 0, sm, p.status)) {
+        if (lane == 0 && wait_bar(smem_u32(&sm.q_ready), 0, sm, p.status, b.wait_ns)) {
             tc_fence_after();
             const uint32_t idesc = idesc_f16(128, p.NP, false, false, false);
             const uint32_t qh = smem_u32(q_hi), ql = smem_u32(q_lo);
@@ -398,8 +399,8 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
                     const uint32_t k = (uint32_t)(i / n_stages);
                     const int buf = i & 1;
                     const uint32_t ka = (uint32_t)(i >> 1);
-                    if (!wait_bar(smem_u32(&sm.acc_empty[buf]), (ka & 1) ^ 1, sm, p.status)) break;
-                    if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status)) break;
+                    if (!wait_bar(smem_u32(&sm.acc_empty[buf]), (ka & 1) ^ 1, sm, p.status, b.wait_ns)) break;
+                    if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status, b.wait_ns)) break;
                     tc_fence_after();
                     if (i == append_tile) patch_append(i, s);
                     issue_step(tmem + (uint32_t)(buf * p.NP), smem_u32(stages + s * kTileBytes), 0);
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
                 for (int i = 0; i < n_mma; ++i) {
                     const int s = i % n_stages;
                     const uint32_t k = (uint32_t)(i / n_stages);
-                    if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status)) break;
+                    if (!wait_bar(smem_u32(&sm.full[s]), k & 1, sm, p.status, b.wait_ns)) break;
                     tc_fence_after();
                     if (i == append_tile) patch_append(i, s);
                     const uint32_t a0 = smem_u32(stages + s * kTileBytes);
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
 #pragma unroll 1
                     for (int h = 0; h < hv; ++h) {
                         const uint32_t u = (uint32_t)(i * hv + h);   // MMA step: accumulator u & 1
-                        if (!wait_bar(smem_u32(&sm.acc_empty[u & 1]), ((u >> 1) & 1) ^ 1, sm, p.status)) {
+                        if (!wait_bar(smem_u32(&sm.acc_empty[u & 1]), ((u >> 1) & 1) ^ 1, sm, p.status, b.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
             const int h = (int)u & (hv - 1);
             const int64_t s = chunk0 + (int64_t)i * kTileKeys + r;
             const int buf = (int)(u & 1);
-            if (!wait_bar(smem_u32(&sm.acc_full[buf]), (u >> 1) & 1, sm, p.status)) {
+            if (!wait_bar(smem_u32(&sm.acc_full[buf]), (u >> 1) & 1, sm, p.status, b.wait_ns)) {
                 aborted = true;
                 break;
             }

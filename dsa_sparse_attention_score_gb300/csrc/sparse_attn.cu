@@ -9,8 +9,10 @@
 //     z_j = sm_scale * (q_lat . c_j[0:512] + q_rope . c_j[512:576]),
 //     o   = sum_j softmax(z)_j c_j[0:512].
 //
-// One CTA per (token, split) handles a run of 64-row tiles of the token's
-// selected positions, with the token's 64 heads on the N side of every MMA:
+// One CTA per (token, head group, split) handles a run of 64-row tiles of the
+// token's selected positions, with a group of 64 of the token's heads on the
+// N side of every MMA (up to 128 heads run as two groups that share nothing
+// but the L2 lines of the gathered rows):
 //     S^T[row, head]  = C[row, 0:576] . Q[head, 0:576]^T        (M=64, N=64, K=576)
 //     O^T[dim, head] += C[row, dim]^T . P^T[row, head]           (M=4x128, N=64, K=64)
 // A gathered tile C sits in shared memory as nine 64-column SWIZZLE_128B
@@ -63,11 +65,12 @@ struct AttnParams {
     const int32_t *idx;
     float *out;
     float *lse;
-    float *part_o;
-    float *part_ml;
+    float *part_o;           // [T, n_split, groups, 64, 512]
+    float *part_ml;          // [T, n_split, groups, 64, 2]
     DevBatch b;
     uint32_t *status;
     int H, k;
+    int groups;              // head groups of 64 per token (1 or 2)
     float scale_log2;        // sm_scale * log2(e)
     int tiles_per_cta, n_split, n_tiles;
     int rope;                // 1: 576-wide rows with the rope tail; 0: 512-wide latent rows
@@ -91,9 +94,10 @@ struct Ctl {
     int32_t warp_alive[4];
 };
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl &c, uint32_t *status) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl &c, uint32_t *status,
+                                         uint64_t limit_ns) {
     if (*(volatile int32_t *)&c.abort_flag) return false;
-    if (mbar_wait(bar, parity)) return true;
+    if (mbar_wait(bar, parity, limit_ns)) return true;
     *(volatile int32_t *)&c.abort_flag = 1;
     flag(status, DSA_DEV_TIMEOUT);
     return false;
@@ -140,9 +144,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DevBatch &b = p.b;
-    const int t = blockIdx.x;
+    const int t = blockIdx.x / p.groups;
+    const int hg = blockIdx.x - t * p.groups;            // head group: heads h0 .. h0 + nh - 1
+    const int h0 = hg * kHeads, nh = min(kHeads, p.H - h0);
     const int split = blockIdx.y;
     if (t >= b.T) return;
+    // this CTA's slice of the split partials
+    const int64_t part = ((int64_t)t * p.n_split + split) * p.groups + hg;
     tl_start(b.timeline, kTlAttn);
     const int pos = __ldg(b.q_pos + t);
     const int seq = seq_of_warp(b.cu_q, b.B, t, lane);
@@ -156,16 +164,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!pos_ok && threadIdx.x == 0 && split == 0) flag(p.status, DSA_DEV_BAD_POSITION);
         // Empty contribution.
         if (p.n_split > 1) {
-            for (int i = threadIdx.x; i < kHeads * D_L; i += kThreads)
-                p.part_o[((int64_t)t * p.n_split + split) * kHeads * D_L + i] = 0.f;
+            for (int i = threadIdx.x; i < kHeads * D_L; i += kThreads) p.part_o[part * kHeads * D_L + i] = 0.f;
             if (threadIdx.x < kHeads) {
-                float *ml = p.part_ml + (((int64_t)t * p.n_split + split) * kHeads + threadIdx.x) * 2;
+                float *ml = p.part_ml + (part * kHeads + threadIdx.x) * 2;
                 ml[0] = -INFINITY;
                 ml[1] = 0.f;
             }
         } else {
-            for (int i = threadIdx.x; i < p.H * D_L; i += kThreads) p.out[(int64_t)t * p.H * D_L + i] = 0.f;
-            if (p.lse && threadIdx.x < p.H) p.lse[(int64_t)t * p.H + threadIdx.x] = -INFINITY;
+            for (int i = threadIdx.x; i < nh * D_L; i += kThreads) p.out[((int64_t)t * p.H + h0) * D_L + i] = 0.f;
+            if (p.lse && threadIdx.x < nh) p.lse[(int64_t)t * p.H + h0 + threadIdx.x] = -INFINITY;
         }
         return;
     }
@@ -203,11 +210,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // A tile is 16 row quads x 9 column blocks = 144 gather4 requests
         // (8 blocks, 128 requests, without the rope tail); producer thread pl
         // sends requests pl and pl + 128.
+        // Under the failure-path test hook nothing is copied, so that the
+        // consumers' waits run out.
         const int pl = (int)threadIdx.x - 32 * (kMmaWarp + 1);
-        if (pl == 0) {
+        const bool copy = !b.skip_copies;
+        if (pl == 0 && copy) {
+            // query rows of the head group; rows past the token's heads (the
+            // next token's, or zero fill past the tensor) only feed padded
+            // accumulator columns that are never stored
             const uint32_t qf = smem_u32(&ctl.q_full);
             mbar_arrive_expect_tx(qf, p.rope ? kQBytes : kQBytes - kQBlockBytes);
-            const int32_t qrow = t * p.H;
+            const int32_t qrow = t * p.H + h0;
             for (int kb = 0; kb < 8; ++kb)
                 tma_load_2d(smem_u32(q_s + kb * kQBlockBytes), &q_lat_map, qf, kb * 64, qrow);
             if (p.rope) tma_load_2d(smem_u32(q_s + 8 * kQBlockBytes), &q_rope_map, qf, 0, qrow);
@@ -247,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rr[u][j] = (int32_t)row;
                 }
             }
-            if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status)) break;
+            if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status, b.wait_ns)) break;
+            if (!copy) continue;
             const uint32_t full = smem_u32(&ctl.c_full[buf]);
             if (pl == 0) mbar_arrive_expect_tx(full, p.rope ? kCBytes : kCBytes - kCBlockBytes);
 #pragma unroll
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // streams are issued in whatever order their inputs arrive, so that an
         // O^T product (which frees a tile buffer for the next gather) never
         // waits behind a gather.
-        if (lane == 0 && wait_bar(smem_u32(&ctl.q_full), 0, ctl, p.status)) {
+        if (lane == 0 && wait_bar(smem_u32(&ctl.q_full), 0, ctl, p.status, b.wait_ns)) {
             const uint32_t id_s = idesc_f16(kRows, kHeads, true, false, false);
             const uint32_t id_o = idesc_f16(128, kHeads, true, true, true);
             const uint32_t qa = smem_u32(q_s), ca = smem_u32(c_s);
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     t_last = global_ns();
                 } else if (*(volatile int32_t *)&ctl.abort_flag) {
                     break;
-                } else if (global_ns() - t_last > kWaitLimitNs) {
+                } else if (global_ns() - t_last > b.wait_ns) {
                     *(volatile int32_t *)&ctl.abort_flag = 1;
                     flag(p.status, DSA_DEV_TIMEOUT);
                     break;
@@ -345,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int e = (tile_lo + it) * kRows + r;
             const int32_t v = e < p.k ? __ldg(idx_row + e) : -1;
             const bool valid = v >= 0 && v <= pos;
-            if (alive) alive = wait_bar(smem_u32(&ctl.s_full[buf]), (uint32_t)(it >> 1) & 1u, ctl, p.status);
+            if (alive) alive = wait_bar(smem_u32(&ctl.s_full[buf]), (uint32_t)(it >> 1) & 1u, ctl, p.status, b.wait_ns);
             alive = __all_sync(0xffffffffu, alive);
             float x[32];
             if (alive) {
@@ -409,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Heads whose maximum moved: rescale their O^T columns once the
                 // previous tile's PV product has landed.  O^T is an M=128
                 // accumulator: every lane of the warp owns one output dim.
-                if (alive) alive = wait_bar(smem_u32(&ctl.o_full), (uint32_t)(it - 1) & 1u, ctl, p.status);
+                if (alive) alive = wait_bar(smem_u32(&ctl.o_full), (uint32_t)(it - 1) & 1u, ctl, p.status, b.wait_ns);
                 alive = __all_sync(0xffffffffu, alive);
                 if (alive) {
                     tc_fence_after();
@@ -435,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&ctl.p_full[buf]));
         }
         // ---- final: O^T of the last tile, row sums, outputs
-        if (alive) alive = wait_bar(smem_u32(&ctl.o_full), (uint32_t)(n_my - 1) & 1u, ctl, p.status);
+        if (alive) alive = wait_bar(smem_u32(&ctl.o_full), (uint32_t)(n_my - 1) & 1u, ctl, p.status, b.wait_ns);
         alive = __all_sync(0xffffffffu, alive);
         float l0, l1;
         half_reduce_32<false>(lpart, lane, l0, l1);
@@ -454,9 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // output otherwise.
             tc_fence_after();
             const int H = p.H;
-            const int rows = p.n_split > 1 ? kHeads : H;
-            float *dst = p.n_split > 1 ? p.part_o + ((int64_t)t * p.n_split + split) * kHeads * D_L
-                                       : p.out + (int64_t)t * H * D_L;
+            const int rows = p.n_split > 1 ? kHeads : nh;
+            float *dst = p.n_split > 1 ? p.part_o + part * kHeads * D_L : p.out + ((int64_t)t * H + h0) * D_L;
             const int rd = quarter * 32 + lane;
             for (int c = 0; c < 4; ++c) {
                 const int d = c * 128 + rd;
@@ -481,11 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = tx;
                 const float l = ctl.l[h], m = ctl.m[h];
                 if (p.n_split > 1) {
-                    float *ml = p.part_ml + (((int64_t)t * p.n_split + split) * kHeads + h) * 2;
+                    float *ml = p.part_ml + (part * kHeads + h) * 2;
                     ml[0] = l > 0.f ? m : -INFINITY;
                     ml[1] = l;
-                } else if (p.lse && h < H) {
-                    p.lse[(int64_t)t * H + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                } else if (p.lse && h < nh) {
+                    p.lse[(int64_t)t * H + h0 + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
                 }
             }
         }
@@ -506,17 +519,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merge split partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const float *__restrict__ part_o,
                                                            const float *__restrict__ part_ml,
-                                                           int n_split, int H, float *out, float *lse,
+                                                           int n_split, int H, int groups, float *out, float *lse,
                                                            unsigned long long *timeline) {
     __shared__ float wgt[128];
     __shared__ float ml[2][128];
     const int t = blockIdx.x, h = blockIdx.y;
-    const int64_t base = (int64_t)t * n_split;
+    // partial row of (split s, head h): ((t * n_split + s) * groups + h / 64) * 64 + h % 64
+    const int64_t hoff = (int64_t)(h / kHeads) * kHeads + h % kHeads;
+    const int64_t stride = (int64_t)groups * kHeads;     // partial rows per split
+    const int64_t base = (int64_t)t * n_split * stride + hoff;
     tl_start(timeline, kTlCombine);
     pdl_wait();
     for (int s = threadIdx.x; s < n_split; s += 128) {      // all split statistics at once
-        ml[0][s] = __ldg(part_ml + ((base + s) * kHeads + h) * 2);
-        ml[1][s] = __ldg(part_ml + ((base + s) * kHeads + h) * 2 + 1);
+        ml[0][s] = __ldg(part_ml + (base + s * stride) * 2);
+        ml[1][s] = __ldg(part_ml + (base + s * stride) * 2 + 1);
     }
     __syncthreads();
     float M = -INFINITY;
@@ -534,7 +550,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float *__restri
 #pragma unroll
         for (int u = 0; u < 16; ++u)
             if (s0 + u < n_split)
-                o[u] = __ldg(reinterpret_cast<const float4 *>(part_o + ((base + s0 + u) * kHeads + h) * D_L) +
+                o[u] = __ldg(reinterpret_cast<const float4 *>(part_o + (base + (s0 + u) * stride) * D_L) +
                              threadIdx.x);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
@@ -570,6 +586,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     p.status = status;
     p.H = a.H;
     p.k = a.k;
+    p.groups = (a.H + kHeads - 1) / kHeads;
     p.scale_log2 = a.sm_scale * 1.4426950408889634f;
     p.tiles_per_cta = a.tiles_per_cta;
     p.n_split = a.n_split;
@@ -578,17 +595,19 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     const size_t smem = sparse_attn_smem_bytes();
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(sparse_attn_kernel), 1, smem);
     if (e != cudaSuccess) return e;
-    if (a.n_split > 65535) return cudaErrorInvalidConfiguration;
-    dim3 grid((unsigned)b.T, (unsigned)a.n_split);
+    if (a.n_split > 65535 || p.groups < 1 || p.groups > 2 || (int64_t)b.T * p.groups > 0x7fffffff)
+        return cudaErrorInvalidConfiguration;
+    dim3 grid((unsigned)(b.T * p.groups), (unsigned)a.n_split);
     return launch_k(sparse_attn_kernel, grid, dim3(kThreads), smem, stream, pdl, p, q_lat_map, q_rope_map, kv_map);
 }
 
 cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStream_t stream, bool pdl) {
     if (a.n_split <= 1) return cudaSuccess;
     if (a.n_split > 128) return cudaErrorInvalidConfiguration;
+    const int groups = (a.H + kHeads - 1) / kHeads;
     dim3 grid((unsigned)b.T, (unsigned)a.H);
     return launch_k(attn_combine_kernel, grid, dim3(128), 0, stream, pdl, (const float *)a.part_o,
-                    (const float *)a.part_ml, a.n_split, a.H, a.out, a.lse, b.timeline);
+                    (const float *)a.part_ml, a.n_split, a.H, groups, a.out, a.lse, b.timeline);
 }
 
 }  // namespace dsa

@@ -36,7 +36,8 @@
  *  - Storage types: dsa_f16 is an IEEE binary16 bit pattern, dsa_bf16 a
  *    bfloat16 bit pattern.  All tensors are dense, row-major, contiguous.
  *  - Fixed dims: indexer head dim 128, latent 512, rope tail 64, row 576.
- *    Supported: 1 <= H_I <= 64 indexer heads, 1 <= H <= 64 query heads,
+ *    Supported: 1 <= H_I <= 64 indexer heads, 1 <= H <= 128 query heads
+ *    (DeepSeek-V3.2, the other model the indexer commit names, has 128),
  *    1 <= k <= 65536.  Others return DSA_ERR_UNSUPPORTED.
  *  - Device pointers passed to the TMA engine (k_cache, kv_cache, q_lat,
  *    q_rope) must be 16-byte aligned, else DSA_ERR_MISALIGNED.
@@ -304,6 +305,8 @@ dsa_status_t dsa_decode_sink(const void *k_new, int k_dtype, const dsa_f16 *q_id
  *    ordering between them) race on it and must not be issued.
  *  - Device-side status bits of these calls accumulate in the array and are
  *    not reported; offending work is still skipped, never trapped.
+ *  - The array's address is looked up once per device and kept: resetting a
+ *    device (cudaDeviceReset) after the first call on it is not supported.
  */
 dsa_status_t dsa_decode_noalloc(const void *k_new, int k_dtype, const dsa_f16 *q_idx, const float *w,
                                 const dsa_bf16 *q_lat, const dsa_bf16 *q_rope,
@@ -361,6 +364,20 @@ dsa_status_t dsa_set_trace_events(cudaEvent_t *events, int n);
  * this leaves the launch order and overlap untouched.  NULL disables it.
  */
 dsa_status_t dsa_set_timeline(void *dev_buf);
+
+/*
+ * Failure-path test hook (not thread-safe; for tests only).  Every bounded
+ * wait in the kernels launched afterwards gives up after wait_limit_ns
+ * nanoseconds (0 restores the default of one second).  With skip_copies set,
+ * the producers of the score and attention kernels issue no copies at all,
+ * so their consumers' first waits run out: the kernels then set
+ * DSA_DEV_TIMEOUT, free their tensor memory and return, with nothing in
+ * flight, and the context stays usable.  Outputs of such calls are
+ * unspecified; the status word reports the timeout.  This exercises the
+ * same code a real stall (a copy that never lands) would take, without
+ * faulting or hanging the GPU.
+ */
+dsa_status_t dsa_set_test_faults(uint64_t wait_limit_ns, int skip_copies);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int dsa_version(void);

@@ -34,6 +34,7 @@ def lib():
             "oracle_k_append": (I32, [P, I32, I32, I32, P, P, P, P, I32]),
             "oracle_indexer_score": (I32, [P, P, P, I32, I32, P, P, P, I32, I32, P, I64]),
             "oracle_topk": (I32, [P, I64, I32, P, I32, P]),
+            "oracle_topk_sink": (I32, [P, I64, I32, P, I32, I32, P, P]),
             "oracle_sparse_attn_f64": (I32, [P, P, P, I32, I32, P, P, P, P, I32, I32, F64, P, P]),
             "oracle_sparse_attn": (I32, [P, P, P, I32, I32, P, P, P, P, I32, I32, F64, P, P]),
             "oracle_sparse_attn_nope_f64": (I32, [P, P, I32, I32, P, P, P, P, I32, I32, F64, P, P]),
@@ -149,18 +150,21 @@ def topk_sink(scores, q_pos, k: int, n_sink: int, seq_of_row=None, anchors=None)
     "UPDATE 6": the sink is anchored on the sequence's first present position.
     Here the boost is taken as unbounded (+inf, which is what +1e20 becomes
     next to float32 scores: the boosted scores tie with one another), then the
-    plain selection runs: ties go to the lower position.
+    plain selection runs: ties go to the lower position (oracle_topk_sink in
+    dsa_oracle.c).
       seq_of_row [T]: sequence of each row (needed with anchors);
       anchors [B]: first present position of each sequence (default 0).
     """
-    s = np.array(scores, dtype=np.float64, copy=True)
-    for r in range(s.shape[0]):
-        a = 0 if anchors is None else int(anchors[int(seq_of_row[r])])
-        lo = max(a, 0)
-        hi = min(a + n_sink, int(q_pos[r]) + 1, s.shape[1])
-        if hi > lo:
-            s[r, lo:hi] = np.inf
-    return topk(s, q_pos, k)
+    s = _c(scores, np.float64)
+    qp = _c(q_pos, np.int32)
+    T = s.shape[0]
+    anchor = None
+    if anchors is not None:
+        anchor = _c([int(anchors[int(seq_of_row[r])]) for r in range(T)], np.int32)
+    idx = np.empty((T, k), np.int32)
+    _check(lib().oracle_topk_sink(_p(s), s.shape[1], T, _p(qp), k, int(n_sink), _p(anchor), _p(idx)),
+           "topk_sink")
+    return idx
 
 
 def sparse_attn(q_lat, q_rope, kv_cache, batch: Batch, idx, sm_scale: float):

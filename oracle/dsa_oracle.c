@@ -242,6 +242,26 @@ int oracle_topk(const double *scores, int64_t ld, int T, const int32_t *q_pos,
 /* ---------------------------------------------------------------- attention */
 
 /* One (token, head): softmax over the listed cache rows, in double. */
+int oracle_topk_sink(const double *scores, int64_t ld, int T, const int32_t *q_pos,
+                     int k, int n_sink, const int32_t *anchor, int32_t *idx)
+{
+    if (n_sink < 0 || T < 0 || ld < 1) return -1;
+    double *boosted = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * (size_t)ld);
+    if (!boosted) return -1;
+    memcpy(boosted, scores, sizeof(double) * (size_t)T * (size_t)ld);
+    for (int t = 0; t < T; t++) {
+        int64_t lo = anchor ? anchor[t] : 0;
+        if (lo < 0) lo = 0;
+        int64_t hi = lo + n_sink;
+        if (hi > (int64_t)q_pos[t] + 1) hi = (int64_t)q_pos[t] + 1;
+        if (hi > ld) hi = ld;
+        for (int64_t s = lo; s < hi; s++) boosted[(int64_t)t * ld + s] = INFINITY;
+    }
+    int rc = oracle_topk(boosted, ld, T, q_pos, k, idx);
+    free(boosted);
+    return rc;
+}
+
 static void attend_rows(const double *ql, const double *qr, const uint16_t *kv_cache,
                         int64_t base, const int32_t *pos, int n, double sm_scale,
                         double *o, double *lse)

@@ -58,6 +58,18 @@ int oracle_indexer_score(const uint16_t *q_idx, const float *w, const uint16_t *
 int oracle_topk(const double *scores, int64_t ld, int T, const int32_t *q_pos,
                 int k, int32_t *idx);
 
+/* Top-k with the attention sink forced in (ik_llama_opt commit log, "GLM-5.2
+ * DSA indexer: decode-correct via persistent indexer-K cache" (attention-sink
+ * force-inclusion), "per-sequence attention sink" and "UPDATE 6 --
+ * serving-correctness"): before the selection, the first n_sink positions of
+ * the row's own sequence, counted from the sequence's first present position
+ * anchor[row] (0 when anchor is NULL), get a boost taken as unbounded: their
+ * scores become +inf, so they rank first and tie among themselves by
+ * position.  Then exactly oracle_topk.  anchor is given per ROW (the caller
+ * maps each row to its sequence's anchor). */
+int oracle_topk_sink(const double *scores, int64_t ld, int T, const int32_t *q_pos,
+                     int k, int n_sink, const int32_t *anchor, int32_t *idx);
+
 /* Sparse MLA attention in the absorbed (latent) form over the selected rows:
  *   z_j = sm_scale * (q_lat[t,h] . c_j[0:512] + q_rope[t,h] . c_j[512:576])
  *   o[t,h] = sum_j softmax(z)_j * c_j[0:512],  lse[t,h] = log sum_j exp(z_j)

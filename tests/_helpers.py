@@ -3,16 +3,23 @@ comparison rules.
 
 Comparison rules (derived from the arithmetic of each path):
   k_append   bit-exact fp16 (both sides round the exact float64 transform once).
-  score      |g - o| <= 1e-3 |o| + 1e-5 A, with A = sum_h |w_h| sum_d |q'_hd k_d|:
-             the relative bound asked for, plus a floor for cancellation that
-             is two orders above the float32 accumulation error over 128
-             products; masked positions must be -inf on both sides.
+  score      |g - o| <= 1e-3 max(|o|, 1e-3 A), with A = sum_h |w_h| ReLU(q'_h . k):
+             1e-3 relative, with a floor for scores that cancel towards zero
+             across heads of both signs; masked positions must be -inf on
+             both sides.  The floor (1e-6 A) sits far above the float32
+             accumulation error of the products but below the error of a
+             rotated query rounded once to fp16, so it tells the hi + lo
+             query of the kernel from a single rounding.
   top-k      bit-exact index set on float32 scores the oracle supplies.
   selection  (end to end) same size; every position in the symmetric
              difference has an oracle score within 1e-3 relative of the
              oracle's k-th score.
-  attention  max |g - o| <= 2e-3 on out, 1e-3 on lse, computed on the
-             GPU's own selection.
+  attention  max |g - o| <= 2e-3 and <= 1e-2 max |o| on out (the outputs of
+             the workloads are small, so the relative bound is the sharper
+             one), max |g - o| <= 1e-3 on lse; computed on the GPU's own
+             selection.
+The achieved worst errors are recorded (ERRORS) and printed at the end of the
+run by conftest.py.
 """
 from __future__ import annotations
 
@@ -41,8 +48,20 @@ def dev_batch(wl):
                                max_q_per_seq=wl.max_q_per_seq, max_kv=wl.max_kv)
 
 
+# worst achieved error of each rule over the run: name -> (error, bound) at
+# the largest error / bound ratio seen
+ERRORS = {}
+
+
+def record(name, err, bound):
+    old = ERRORS.get(name)
+    if old is None or err / bound > old[0] / old[1]:
+        ERRORS[name] = (float(err), float(bound))
+
+
 def score_tolerance(q_idx, w, k_cache, wl, t, hadamard):
-    """Per-position absolute tolerance of row t (float64 array over 0..p_t)."""
+    """A = sum_h |w_h| ReLU(q'_h . k_s) for each visible position s of row t
+    (float64 array over 0..p_t), q' the (rotated) query in float64."""
     import scipy.linalg
     b = int(np.searchsorted(wl.cu_q, t, side="right") - 1)
     p = wl.q_pos[t]
@@ -50,18 +69,44 @@ def score_tolerance(q_idx, w, k_cache, wl, t, hadamard):
     q = q_idx[t].astype(np.float64)
     if hadamard:
         q = q @ (scipy.linalg.hadamard(128) / np.sqrt(128)).T
-    k = np.abs(k_cache[off:off + p + 1].astype(np.float64))
-    A = np.abs(w[t].astype(np.float64)) @ (np.abs(q) @ k.T)
-    return A
+    k = k_cache[off:off + p + 1].astype(np.float64)
+    return np.abs(w[t].astype(np.float64)) @ np.maximum(q @ k.T, 0.0)
 
 
-def check_scores(got, ref, A):
+def score_bound(ref, A):
+    return 1e-3 * np.maximum(np.abs(ref), 1e-3 * A)
+
+
+def check_scores(got, ref, A, name="score"):
     """got/ref over the visible range of one row; A per position."""
     err = np.abs(got.astype(np.float64) - ref)
-    tol = 1e-3 * np.abs(ref) + 1e-5 * A
+    tol = score_bound(ref, A)
     bad = np.nonzero(err > tol)[0]
     assert bad.size == 0, f"{bad.size} scores out of tolerance, first {bad[:5]}: " \
                           f"got {got[bad[:5]]} ref {ref[bad[:5]]} tol {tol[bad[:5]]}"
+    if err.size:
+        i = int(np.argmax(err / tol))
+        record(name, err[i], tol[i])
+
+
+def check_attention(go, gl, ref_o, ref_l, name="attention", lse_tol=1e-3):
+    """Output and lse rule: max |g - o| <= min(2e-3, 1e-2 max |o|) on the
+    output, <= lse_tol (1e-3) on the (finite) lse."""
+    err_o = float(np.abs(go - ref_o).max()) if go.size else 0.0
+    bound_o = min(2e-3, 1e-2 * float(np.abs(ref_o).max())) if go.size else 1.0
+    if bound_o == 0.0:                      # all-zero reference (empty selections)
+        assert err_o == 0.0, err_o
+    else:
+        assert err_o <= bound_o, (err_o, bound_o)
+        record(name + " out", err_o, bound_o)
+    if gl is not None:
+        fin = np.isfinite(ref_l)
+        assert np.array_equal(np.isfinite(gl), fin)
+        if fin.any():
+            err_l = float(np.abs(gl[fin] - ref_l[fin]).max())
+            assert err_l <= lse_tol, err_l
+            record(name + " lse", err_l, lse_tol)
+    return err_o
 
 
 def check_selection(gpu_idx, ref_idx, ref_scores, k):

@@ -25,3 +25,16 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Worst achieved error of each parity rule in this run (GPU runs)."""
+    try:
+        from _helpers import ERRORS
+    except ImportError:  # pragma: no cover
+        return
+    if not ERRORS:
+        return
+    terminalreporter.write_line("parity: worst achieved error / bound per rule")
+    for name, (err, bound) in sorted(ERRORS.items()):
+        terminalreporter.write_line(f"  {name:32s} {err:.3e} / {bound:.3e} = {err / bound:.3f}")

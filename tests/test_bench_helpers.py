@@ -46,3 +46,46 @@ def test_cpu_baseline_is_bounded_and_reports_one_thread():
     subs = bench.token_subs(wl, inp, [0, 129])
     assert [o.q_pos for o, _ in subs] == [[200], [329]]
     assert subs[1][1].k_cache.shape[0] == 330
+
+
+def test_exclusive_spans_split_an_overlapped_step():
+    """Kernels that start early (programmatic dependent launch) and wait for
+    their predecessor are charged from the predecessor's end; the shares add
+    up to the step's span."""
+    spans = {"indexer_score": (0.0, 9.26), "topk": (3.46, 17.12), "sparse_attn": (7.5, 30.11),
+             "attn_combine": (30.78, 35.6)}
+    ex = bench.exclusive_spans(spans)
+    assert ex == pytest.approx({"indexer_score": 9.26, "topk": 7.86, "sparse_attn": 12.99, "attn_combine": 4.82})
+    assert sum(ex.values()) == pytest.approx(35.6 - 0.67)     # the gap before the combine is nobody's
+    # a kernel that starts after its predecessor ends keeps its own span
+    assert bench.exclusive_spans({"k_append": (0, 1), "indexer_score": (2, 5)}) == {"k_append": 1, "indexer_score": 3}
+
+
+def test_kernel_rooflines_follow_the_workload_kind():
+    import dsa_synth as S
+    pk = dict(hbm_gbs=6000.0, bf16_tflops=2000.0, bf16_tflops_sustained=1800.0)
+    dec, pre = S.config(2), S.config(4)
+    a_dec, a_pre = bench.algorithmic(dec), bench.algorithmic(pre)
+    r = bench.kernel_roofline("sparse_attn", 0.010, dec, a_dec, pk)
+    assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(8 * 2048 * 1152 / 1e-5 / 1e9)
+    r = bench.kernel_roofline("indexer_score", 0.4, pre, a_pre, pk)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["algorithmic_flops"] == 25167872 * 64 * 256                  # causal pairs x heads x 2*128
+    assert r["frac"] == pytest.approx(r["achieved"] / 2000.0)
+    r = bench.kernel_roofline("sparse_attn", 3.0, pre, a_pre, pk)
+    assert r["bound"] == "tensor" and r["algorithmic_flops"] == 4096 * 2048 * 64 * 2 * 1088
+
+
+def test_score_windows_from_the_launch_count():
+    class Fake:
+        def __init__(self, n):
+            self.n = n
+
+        def dsa_decode_launches(self, batch, H_I, H, k):
+            return self.n
+
+    class B:
+        max_q_per_seq = 1
+    assert bench.score_windows(Fake(3), B()) == 1              # score, top-k, attention
+    B.max_q_per_seq = 16384
+    assert bench.score_windows(Fake(18), B()) == 8             # append + 8 x (score, top-k) + attention

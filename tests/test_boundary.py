@@ -59,7 +59,7 @@ def test_device_status_bits_match_the_header():
 
 
 def test_version_and_status_strings(L):
-    assert dsa.dsa_version() == 10000
+    assert dsa.dsa_version() == 10100
     for code in range(0, 7):
         assert dsa.dsa_status_string(code) not in ("", "unknown status")
     assert dsa.dsa_status_string(99) == "unknown status"
@@ -85,6 +85,34 @@ def test_workspace_sizes(L):
     assert L.dsa_workspace_size(7, C.byref(b), 32, 64, 16, C.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
     assert L.dsa_workspace_size(dsa.DSA_OP_TOPK, C.byref(b), 32, 64, 0, C.byref(n)) == dsa.DSA_ERR_UNSUPPORTED
     assert L.dsa_workspace_size(0, None, 32, 64, 16, C.byref(n)) == dsa.DSA_ERR_INVALID_ARGUMENT
+
+
+def test_split_partials_stay_within_what_the_combine_merges(L):
+    """One token with k = 65536 (1024 row tiles) would ask for 147 splits;
+    the layout caps them at the 128 the combine kernel merges, so the
+    workspace holds exactly 128 partials of 64 heads (plus their (m, l))."""
+    n = C.c_size_t()
+    b = _batch(batch=1, total_q=1, max_kv=70000, cache_rows=70000)
+    assert L.dsa_workspace_size(dsa.DSA_OP_SPARSE_ATTN, C.byref(b), 4, 8, 65536, C.byref(n)) == dsa.DSA_OK
+    part_o, part_ml = 128 * 64 * 512 * 4, 128 * 64 * 2 * 4
+    assert n.value == 256 + part_o + part_ml
+
+
+def test_head_groups_size_the_partials(L):
+    """More than 64 query heads run as two head groups of 64; the split
+    partials hold both groups (8 tokens x 128 heads: 8 splits of 4 tiles)."""
+    n = C.c_size_t()
+    b = _batch(batch=8, total_q=8, max_kv=8192, cache_rows=8 * 8192)
+    assert L.dsa_workspace_size(dsa.DSA_OP_SPARSE_ATTN, C.byref(b), 64, 128, 2048, C.byref(n)) == dsa.DSA_OK
+    rows = 8 * 8 * 2 * 64
+    assert n.value == 256 + rows * 512 * 4 + rows * 2 * 4
+    assert L.dsa_workspace_size(dsa.DSA_OP_SPARSE_ATTN, C.byref(b), 64, 129, 2048, C.byref(n)) == \
+        dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_test_fault_hook_is_a_host_setting(L):
+    assert L.dsa_set_test_faults(2_000_000, 1) == dsa.DSA_OK
+    assert L.dsa_set_test_faults(0, 0) == dsa.DSA_OK
 
 
 def test_decode_launch_counts(L):
@@ -122,8 +150,12 @@ def test_argument_validation_runs_before_any_launch(L):
         dsa.DSA_ERR_UNSUPPORTED
     assert L.dsa_topk(fake, 100, C.byref(b), 0, fake, ws, nws, None) == dsa.DSA_ERR_UNSUPPORTED
     assert L.dsa_topk(fake, 100, C.byref(b), 70000, fake, ws, nws, None) == dsa.DSA_ERR_UNSUPPORTED
-    assert L.dsa_sparse_mla_attn(fake, fake, fake, C.byref(b), fake, 16, 65, 0.1, fake, None, ws, nws,
+    assert L.dsa_sparse_mla_attn(fake, fake, fake, C.byref(b), fake, 16, 129, 0.1, fake, None, ws, nws,
                                  None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_sparse_mla_attn(fake, fake, fake, C.byref(b), fake, 16, 0, 0.1, fake, None, ws, nws,
+                                 None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_decode(fake, 0, fake, fake, fake, fake, fake, fake, C.byref(b), 32, 129, 16, 0.1, 0,
+                        fake, None, None, ws, nws, None) == dsa.DSA_ERR_UNSUPPORTED
     # score row stride shorter than the visible span
     assert L.dsa_topk(fake, 99, C.byref(b), 4, fake, ws, nws, None) == dsa.DSA_ERR_INVALID_ARGUMENT
     # misaligned TMA operands

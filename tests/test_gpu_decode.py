@@ -10,7 +10,7 @@ import pytest
 
 import dsa_synth as S
 import oracle
-from _helpers import assert_sorted_unique, check_selection, dev_batch, to_dev
+from _helpers import assert_sorted_unique, check_attention, check_selection, dev_batch, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -58,10 +58,7 @@ def check_rows(wl, inp, g, rows, kc_ref):
         swaps += check_selection(g["idx"][t], ref_idx[i], scores[i, :n], wl.top_k)
     ref_o, ref_l = oracle.sparse_attn(inp.q_lat[rows], inp.q_rope[rows], inp.kv_cache, sub,
                                       g["idx"][rows], wl.sm_scale)
-    err_o = np.abs(g["out"][rows] - ref_o).max()
-    err_l = np.abs(g["lse"][rows] - ref_l).max()
-    assert err_o <= 2e-3, err_o
-    assert err_l <= 1e-3, err_l
+    check_attention(g["out"][rows], g["lse"][rows], ref_o, ref_l, name="decode attention")
     return swaps
 
 
@@ -89,8 +86,7 @@ def test_tiny_decode_dense_equivalence_k256(dsa):
     ql = S.bf16_bits_to_f32(inp.q_lat).astype(np.float64)
     qr = S.bf16_bits_to_f32(inp.q_rope).astype(np.float64)
     de, dl = oracle.dense_attn_f64(ql, qr, inp.kv_cache, oracle.Batch.of(wl), wl.sm_scale)
-    assert np.abs(g["out"] - de).max() <= 2e-3
-    assert np.abs(g["lse"] - dl).max() <= 1e-3
+    check_attention(g["out"], g["lse"], de, dl, name="dense equivalence")
 
 
 def test_tiny_decode_hadamard(dsa):
@@ -113,6 +109,20 @@ def test_long_prefill_sampled(dsa):
     check_workload(dsa, S.config(5), sample=True)
 
 
+def test_deepseek_shaped_decode_128_heads(dsa):
+    """128 query heads (DeepSeek-V3.2, the other model of the indexer commit):
+    two head groups of 64 per token, split across CTAs and combined."""
+    wl = S.decode_workload("ds128", 52, [8192, 5000, 3001, 2048], H_I=64, H=128, top_k=2048)
+    check_workload(dsa, wl)
+
+
+def test_one_token_attends_65536_rows(dsa):
+    """k = 65536 for a single token: 1024 row tiles, which would ask for more
+    split partials than the combine merges; the split is capped at 128."""
+    wl = S.decode_workload("k64k", 53, [70000], H_I=4, H=8, top_k=65536)
+    check_workload(dsa, wl)
+
+
 def test_multi_sequence_prefill_chunks(dsa):
     """Two sequences with several query tokens each (varlen), mixed lengths."""
     wl = S.Workload("mixed", 51, kv_len=[700, 3000], q_pos=[680 + i for i in range(20)] + [2990 + i for i in range(10)],
@@ -132,12 +142,10 @@ def _decode_on(dsa, wl, inp, b, ws, kc, kv):
 
 
 def test_decode_steps_reuse_workspace(dsa):
-    """Consecutive single-token steps on one workspace.  Decode batches select
-    inside the score kernel with per-sequence histograms and counters kept in
-    the workspace; they must be back at zero after every call.  The rows cover
-    n < k, n == k, n == k + 1, rows that fit the kernel's shared-memory key
-    scratch and rows longer than it, and sequences scored by one CTA and by
-    many."""
+    """Consecutive single-token steps on one workspace, whose score slab,
+    index rows and split partials each step overwrites.  The rows cover
+    n < k, n == k, n == k + 1, rows that one top-k CTA holds in registers and
+    rows spread over a cluster, and sequences scored by one CTA and by many."""
     kv_len = [40000, 3000, 2049, 70000, 200]
     steps = [[38990, 1000, 2046, 68990, 10],
              [38991, 1001, 2047, 68991, 11],

@@ -10,7 +10,7 @@ import pytest
 
 import dsa_synth as S
 import oracle
-from _helpers import dev_batch, to_dev
+from _helpers import check_attention, dev_batch, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +52,5 @@ def test_shared_layer_reuses_full_layer_selection():
                                     wl.sm_scale, out, lse, ws)
             ref_o, ref_l = oracle.sparse_attn(inp.q_lat, inp.q_rope, inp.kv_cache, oracle.Batch.of(wl),
                                               last_full, wl.sm_scale)
-            assert np.abs(out.cpu().numpy() - ref_o).max() <= 2e-3
-            assert np.abs(lse.cpu().numpy() - ref_l).max() <= 1e-3
+            check_attention(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, name="indexshare attention")
         assert dsa.dsa_read_device_status(ws) == 0

@@ -6,14 +6,14 @@ Each sequence's logical rows are scattered into a pooled cache of shuffled
 physical blocks whose unused rows hold large garbage values;
 dsa_decode_paged on the pool must match the oracle on the logical,
 contiguous arrays: the appended key bit-exact at its physical row, the
-selection by the decode tests' rule, attention within 2e-3 / 1e-3.
+selection by the decode tests' rule, attention by the shared attention rule.
 """
 import numpy as np
 import pytest
 
 import dsa_synth as S
 import oracle
-from _helpers import assert_sorted_unique, check_selection, to_dev
+from _helpers import assert_sorted_unique, check_attention, check_selection, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -97,8 +97,7 @@ def test_paged_decode_matches_oracle(dsa, name, bs, wl):
         assert_sorted_unique(g_idx[t], n)
         check_selection(g_idx[t], ref_idx[t], scores[t, :n], wl.top_k)
     ref_o, ref_l = oracle.sparse_attn(inp.q_lat, inp.q_rope, inp.kv_cache, ob, g_idx, wl.sm_scale)
-    assert np.abs(g_out - ref_o).max() <= 2e-3
-    assert np.abs(g_lse - ref_l).max() <= 1e-3
+    check_attention(g_out, g_lse, ref_o, ref_l, name="paged attention")
 
 
 def test_paged_rejects_bad_block_size(dsa):

@@ -13,7 +13,7 @@ import pytest
 
 import dsa_synth as S
 import oracle
-from _helpers import assert_sorted_unique, check_selection, dev_batch, to_dev
+from _helpers import assert_sorted_unique, check_attention, check_selection, dev_batch, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -103,5 +103,4 @@ def test_decode_sink_end_to_end(dsa):
         assert set(range(anchors[t], anchors[t] + n_sink)) <= set(g_idx[t].tolist())
         check_selection(g_idx[t], ref[t], boosted[t, :n], wl.top_k)
     ref_o, ref_l = oracle.sparse_attn(inp.q_lat, inp.q_rope, inp.kv_cache, ob, g_idx, wl.sm_scale)
-    assert np.abs(g_out - ref_o).max() <= 2e-3
-    assert np.abs(g_lse - ref_l).max() <= 1e-3
+    check_attention(g_out, g_lse, ref_o, ref_l, name="sink attention")

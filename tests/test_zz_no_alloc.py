@@ -1,10 +1,11 @@
 """dsa_decode_noalloc: the decode step for callers that cannot allocate device
 memory (no workspace argument; the library's static scratch is used instead).
 
-Checked through the C ABI against dsa_decode with a caller workspace, on two
-calls in a row, within the tolerances of the other GPU tests (attention output
-2e-3 max-abs, lse 1e-3; indices and appended keys exact).  This file is named
-so that pytest collects it last.
+Checked against dsa_decode with a caller workspace on two calls in a row
+(the first through the raw C ABI, the second through the Python binding),
+within the tolerances of the other GPU tests (attention output 2e-3
+max-abs, lse 1e-3; indices and appended keys exact).  This file is named so
+that pytest collects it last.
 """
 import ctypes as C
 
@@ -55,10 +56,13 @@ def test_noalloc_matches_workspace_decode_twice(dsa):
     for call in range(2):
         kc = to_dev(inp.k_cache)
         out, lse, idx = outputs()
-        rc = L.dsa_decode_noalloc(_p(args[0]), dsa.DSA_KEY_F32, _p(args[1]), _p(args[2]), _p(args[3]),
-                                  _p(args[4]), _p(kc), _p(kv), C.byref(desc), wl.H_I, wl.H, wl.top_k,
-                                  C.c_float(wl.sm_scale), int(wl.hadamard), _p(out), _p(lse), _p(idx), stream)
-        assert rc == dsa.DSA_OK, dsa.dsa_status_string(rc)
+        if call == 0:                                  # the raw C ABI
+            rc = L.dsa_decode_noalloc(_p(args[0]), dsa.DSA_KEY_F32, _p(args[1]), _p(args[2]), _p(args[3]),
+                                      _p(args[4]), _p(kc), _p(kv), C.byref(desc), wl.H_I, wl.H, wl.top_k,
+                                      C.c_float(wl.sm_scale), int(wl.hadamard), _p(out), _p(lse), _p(idx), stream)
+            assert rc == dsa.DSA_OK, dsa.dsa_status_string(rc)
+        else:                                          # the Python binding of the same call
+            dsa.dsa_decode_noalloc(*args, kc, kv, b, wl.top_k, wl.sm_scale, wl.hadamard, out, lse, idx)
         torch.cuda.synchronize()
         assert torch.equal(kc, kc_ref), f"call {call}: appended keys differ"
         assert torch.equal(idx, idx_ref), f"call {call}: selections differ"
