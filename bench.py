@@ -686,6 +686,9 @@ def measure(dsa, torch, wl, steps, warmup, flush_mb, world=1, e2e_steps=0, graph
                   f"median of {n_side} steps")
     else:
         kernel_ms = {st: statistics.median(v) for st, v in stage_ms.items() if v and statistics.median(v) > 0}
+        append = 0 if wl.max_q_per_seq == 1 else 1
+        if launches - append - 2 * windows - 1 == 0:    # no split tokens: no combine kernel ran
+            kernel_ms.pop("attn_combine", None)
         source = (f"stage events around each of the {windows} score windows' top-k launches (the score and "
                   f"top-k kernels alternate, so their timeline spans overlap); median of {n_side} steps")
 

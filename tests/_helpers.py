@@ -54,6 +54,8 @@ ERRORS = {}
 
 
 def record(name, err, bound):
+    if not bound > 0 or not np.isfinite(bound):
+        return
     old = ERRORS.get(name)
     if old is None or err / bound > old[0] / old[1]:
         ERRORS[name] = (float(err), float(bound))
@@ -84,8 +86,9 @@ def check_scores(got, ref, A, name="score"):
     bad = np.nonzero(err > tol)[0]
     assert bad.size == 0, f"{bad.size} scores out of tolerance, first {bad[:5]}: " \
                           f"got {got[bad[:5]]} ref {ref[bad[:5]]} tol {tol[bad[:5]]}"
-    if err.size:
-        i = int(np.argmax(err / tol))
+    pos = tol > 0
+    if pos.any():
+        i = int(np.argmax(np.where(pos, err / np.where(pos, tol, 1.0), -1.0)))
         record(name, err[i], tol[i])
 
 
