@@ -198,6 +198,7 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
         return DSA_ERR_CUDA;
     AttnLaunch a{};
     a.rope = rope ? 1 : 0;
+    a.kv = kv_cache;
     a.H = H;
     a.k = k;
     a.sm_scale = sm_scale;

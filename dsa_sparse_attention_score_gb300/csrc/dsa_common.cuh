@@ -210,6 +210,17 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 only (cp.async.cg),
+// tracked by the issuing thread's cp.async groups.  Both addresses 16-byte
+// aligned.  The data is written through the generic proxy: before the
+// tensor core reads it, the writer waits for its copies and issues
+// fence.proxy.async.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Bulk copy shared -> global (TMA), tracked by a bulk group of this thread.
 __device__ __forceinline__ void bulk_s2g(void *gdst, uint32_t ssrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)

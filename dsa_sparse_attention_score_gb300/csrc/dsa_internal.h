@@ -114,6 +114,7 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
 
 struct AttnLaunch {
     int rope = 1;            // 0: 512-wide latent rows without the rope tail
+    const void *kv;          // the latent cache: [cache_rows, 576] (or 512) bf16
     int H, k;
     float sm_scale;
     const int32_t *idx;      // [T, k]

@@ -62,6 +62,7 @@ constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
 
 struct AttnParams {
+    const uint8_t *kv;       // the latent cache (16-byte aligned rows), for the cp.async gather
     const int32_t *idx;
     float *out;
     float *lse;
@@ -74,6 +75,7 @@ struct AttnParams {
     float scale_log2;        // sm_scale * log2(e)
     int tiles_per_cta, n_split, n_tiles;
     int rope;                // 1: 576-wide rows with the rope tail; 0: 512-wide latent rows
+    int async_copy;          // gather rows with cp.async (1) or TMA tile::gather4 (0)
 };
 
 struct Ctl {
@@ -129,6 +131,24 @@ __device__ __forceinline__ void half_reduce_32(const float (&x)[32], int lane, f
     r1 = a[1];
 }
 
+// One producer warp copies 16 rows of a tile (tile rows r0 .. r0 + 15) whose
+// cache rows lanes 0..15 hold in my_row, CPR 16-byte chunks per row (72 with
+// the rope tail, 64 without), into the nine-block SWIZZLE_128B layout the
+// MMAs read.  Instruction j of lane l copies flat chunk 32 j + l of the
+// warp's 16 x CPR chunks, so every warp instruction reads at most two rows'
+// contiguous runs of bytes.
+template <int CPR>
+__device__ __forceinline__ void copy_rows16(uint32_t cb, const uint8_t *kv, int32_t my_row, int r0, int lane) {
+#pragma unroll 4
+    for (int j = 0; j < CPR / 2; ++j) {
+        const int f = j * 32 + lane;
+        const int rl = f / CPR, c = f - rl * CPR;
+        const int32_t row = __shfl_sync(0xffffffffu, my_row, rl);
+        const uint32_t dst = cb + (uint32_t)(c >> 3) * kCBlockBytes + sw128_offset((uint32_t)(r0 + rl), (uint32_t)(c & 7));
+        cp_async16(dst, kv + (int64_t)row * (CPR * 16) + c * 16);
+    }
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -181,7 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&ctl.q_full), 1);
         for (int i = 0; i < kBufs; ++i) {
-            mbar_init(smem_u32(&ctl.c_full[i]), 1);
+            // a tile lands when its bytes arrive (TMA) or when every producer
+            // has seen its own copies complete (cp.async)
+            mbar_init(smem_u32(&ctl.c_full[i]), p.async_copy ? kProducers : 1);
             mbar_init(smem_u32(&ctl.c_empty[i]), 1);
             mbar_init(smem_u32(&ctl.s_full[i]), 1);
             mbar_init(smem_u32(&ctl.p_full[i]), kSoftmaxWarps);
@@ -225,52 +247,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem_u32(q_s + kb * kQBlockBytes), &q_lat_map, qf, kb * 64, qrow);
             if (p.rope) tma_load_2d(smem_u32(q_s + 8 * kQBlockBytes), &q_rope_map, qf, 0, qrow);
         }
-        const int nb = p.rope ? kBlocks : kBlocks - 1;   // column blocks gathered per row
-        const int n_req = (kRows / 4) * nb;                // gather4 requests per tile
-        pdl_wait();                                  // the indices come from the preceding kernel
-        // Rows of this thread's requests (at most two: 144 per tile, 128
-        // producers) are looked up before the buffer is free, so the copies
-        // go out as soon as it is.
-        constexpr int kReq = ((kRows / 4) * kBlocks + kProducers - 1) / kProducers;
-        for (int it = 0; it < n_my; ++it) {
-            const int buf = it & 1;
-            const uint32_t use = (uint32_t)(it >> 1);
-            int32_t rr[kReq][4];
-#pragma unroll
-            for (int u = 0; u < kReq; ++u) {
-                const int q = pl + u * kProducers;
-                if (q >= n_req) break;
-                const int quad = p.rope ? q / kBlocks : q >> 3, kb = p.rope ? q % kBlocks : q & 7;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int e = (tile_lo + it) * kRows + quad * 4 + j;
-                    const int32_t v = e < p.k ? __ldg(idx_row + e) : -1;
-                    bool ok = v >= 0 && v <= pos;
-                    int64_t row;
-                    if (!b.block_table) {
-                        row = kv0 + (ok ? v : pos);      // in range: the position check covers v <= pos
-                    } else {
-                        row = ok ? cache_row(b, seq, kv0, v) : own_row;
-                        if (row < 0 || row >= b.cache_rows) {
-                            ok = false;
-                            row = own_row;
-                        }
-                    }
-                    if (!ok && v != -1 && kb == 0) flag(p.status, DSA_DEV_BAD_INDEX);
-                    rr[u][j] = (int32_t)row;
+        // Cache row of entry e of the token's index row: the row itself when it
+        // is a visible position, else (padding, or out of range: flagged) the
+        // token's own row, whose scores the softmax masks.
+        auto row_of = [&](int e, bool report) -> int32_t {
+            const int32_t v = e < p.k ? __ldg(idx_row + e) : -1;
+            bool ok = v >= 0 && v <= pos;
+            int64_t row;
+            if (!b.block_table) {
+                row = kv0 + (ok ? v : pos);          // in range: the position check covers v <= pos
+            } else {
+                row = ok ? cache_row(b, seq, kv0, v) : own_row;
+                if (row < 0 || row >= b.cache_rows) {
+                    ok = false;
+                    row = own_row;
                 }
             }
-            if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status, b.wait_ns)) break;
-            if (!copy) continue;
-            const uint32_t full = smem_u32(&ctl.c_full[buf]);
-            if (pl == 0) mbar_arrive_expect_tx(full, p.rope ? kCBytes : kCBytes - kCBlockBytes);
+            if (!ok && v != -1 && report) flag(p.status, DSA_DEV_BAD_INDEX);
+            return (int32_t)row;
+        };
+        pdl_wait();                                  // the indices come from the preceding kernel
+        if (p.async_copy) {
+            // cp.async gather: warp pw copies tile rows 16 pw .. 16 pw + 15,
+            // then waits for its own copies, fences them for the tensor core
+            // and arrives; the tile is full when all 128 producers have.
+            const int pw = pl >> 5;
+            for (int it = 0; it < n_my; ++it) {
+                const int buf = it & 1;
+                const uint32_t use = (uint32_t)(it >> 1);
+                const int32_t my_row = lane < 16 ? row_of((tile_lo + it) * kRows + 16 * pw + lane, true) : 0;
+                if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status, b.wait_ns)) break;
+                if (!copy) continue;
+                const uint32_t cb = smem_u32(c_s + buf * kCBytes);
+                if (p.rope) copy_rows16<kBlocks * 8>(cb, p.kv, my_row, 16 * pw, lane);
+                else copy_rows16<(kBlocks - 1) * 8>(cb, p.kv, my_row, 16 * pw, lane);
+                cp_async_commit();
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&ctl.c_full[buf]));
+            }
+        } else {
+            // TMA gather: a tile is 16 row quads x 9 column blocks = 144
+            // gather4 requests (8 blocks, 128 requests, without the rope
+            // tail); producer thread pl sends requests pl and pl + 128.  Their
+            // rows are looked up before the buffer is free, so the copies go
+            // out as soon as it is.
+            const int nb = p.rope ? kBlocks : kBlocks - 1;   // column blocks gathered per row
+            const int n_req = (kRows / 4) * nb;                // gather4 requests per tile
+            constexpr int kReq = ((kRows / 4) * kBlocks + kProducers - 1) / kProducers;
+            for (int it = 0; it < n_my; ++it) {
+                const int buf = it & 1;
+                const uint32_t use = (uint32_t)(it >> 1);
+                int32_t rr[kReq][4];
 #pragma unroll
-            for (int u = 0; u < kReq; ++u) {
-                const int q = pl + u * kProducers;
-                if (q >= n_req) break;
-                const int quad = p.rope ? q / kBlocks : q >> 3, kb = p.rope ? q % kBlocks : q & 7;
-                tma_gather4(smem_u32(c_s + buf * kCBytes + kb * kCBlockBytes + quad * 512), &kv_map, full, kb * 64,
-                            rr[u][0], rr[u][1], rr[u][2], rr[u][3]);
+                for (int u = 0; u < kReq; ++u) {
+                    const int q = pl + u * kProducers;
+                    if (q >= n_req) break;
+                    const int quad = p.rope ? q / kBlocks : q >> 3, kb = p.rope ? q % kBlocks : q & 7;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) rr[u][j] = row_of((tile_lo + it) * kRows + quad * 4 + j, kb == 0);
+                }
+                if (!wait_bar(smem_u32(&ctl.c_empty[buf]), (use & 1u) ^ 1u, ctl, p.status, b.wait_ns)) break;
+                if (!copy) continue;
+                const uint32_t full = smem_u32(&ctl.c_full[buf]);
+                if (pl == 0) mbar_arrive_expect_tx(full, p.rope ? kCBytes : kCBytes - kCBlockBytes);
+#pragma unroll
+                for (int u = 0; u < kReq; ++u) {
+                    const int q = pl + u * kProducers;
+                    if (q >= n_req) break;
+                    const int quad = p.rope ? q / kBlocks : q >> 3, kb = p.rope ? q % kBlocks : q & 7;
+                    tma_gather4(smem_u32(c_s + buf * kCBytes + kb * kCBlockBytes + quad * 512), &kv_map, full,
+                                kb * 64, rr[u][0], rr[u][1], rr[u][2], rr[u][3]);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -577,6 +625,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
                                const CUtensorMap &q_rope_map, const CUtensorMap &kv_map,
                                const DevBatch &b, uint32_t *status, cudaStream_t stream, bool pdl) {
     AttnParams p{};
+    p.kv = static_cast<const uint8_t *>(a.kv);
     p.idx = a.idx;
     p.out = a.out;
     p.lse = a.lse;
@@ -592,6 +641,9 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     p.n_split = a.n_split;
     p.n_tiles = (a.k + kRows - 1) / kRows;
     p.rope = a.rope;
+    // Gather path: cp.async reads each row through L2 at the load/store
+    // units' rate; TMA tile::gather4 issues one 512-byte request at a time.
+    p.async_copy = 1;
     const size_t smem = sparse_attn_smem_bytes();
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(sparse_attn_kernel), 1, smem);
     if (e != cudaSuccess) return e;
