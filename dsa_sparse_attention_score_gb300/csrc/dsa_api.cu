@@ -142,7 +142,7 @@ Layout layout(int op, const dsa_batch_t *b, int H, int k) {
         if (L.n_split > 1) {
             const size_t rows = (size_t)b->total_q * L.n_split * head_groups(H) * 64;
             L.part_o = off;
-            L.part_o_bytes = rows * D_L * 4;
+            L.part_o_bytes = rows * D_L * 2;           // bf16
             off = align_up(off + L.part_o_bytes, kAlign);
             L.part_ml = off;
             L.part_ml_bytes = rows * 2 * 4;
@@ -208,7 +208,7 @@ dsa_status_t run_attention(const dsa_bf16 *q_lat, const dsa_bf16 *q_rope, const 
     a.n_split = L.n_split;
     a.tiles_per_cta = L.tiles_per_cta;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
-    a.part_o = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_o) : nullptr;
+    a.part_o = L.n_split > 1 ? static_cast<void *>(w8 + L.part_o) : nullptr;
     a.part_ml = L.n_split > 1 ? reinterpret_cast<float *>(w8 + L.part_ml) : nullptr;
     DSA_TRY_CUDA(launch_sparse_attn(a, ql, qr, kv, db, status_ptr(ws), stream, pdl));
     if (traced) trace(4, stream);

@@ -61,9 +61,11 @@ __device__ __forceinline__ int seq_of(const int32_t *cu_q, int B, int t) {
 }
 
 // ---------------------------------------------------------------- time
+// The memory clobber keeps the read where it is written: the compiler may
+// not move it across barriers or memory operations.
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t) : : "memory");
     return t;
 }
 // Every wait inside a CTA is bounded, by default by this; a wait that runs

@@ -122,7 +122,7 @@ struct AttnLaunch {
     float *lse;              // [T, H] or null
     int tiles_per_cta;       // attention row tiles handled by one CTA
     int n_split;             // CTAs per (token, head group)
-    float *part_o;           // [T, n_split, groups*64, 512] when n_split > 1
+    void *part_o;            // bf16 [T, n_split, groups*64, 512] when n_split > 1
     float *part_ml;          // [T, n_split, groups*64, 2]
 };
 cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map,

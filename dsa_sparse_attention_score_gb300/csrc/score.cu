@@ -535,6 +535,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     }
 
     tc_fence_before();
+    __syncwarp();                  // lanes of warps 0 and 1 arrive from different paths
     __syncthreads();
     if (!p.early) pdl_trigger();   // late: waiting dependents would share the SMs
     tl_end(b.timeline, kTlScore);

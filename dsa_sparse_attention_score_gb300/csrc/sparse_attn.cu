@@ -33,9 +33,10 @@
 // read by the two halves of the warp for heads 0..31 and 32..63.
 // The per-head running maximum is only raised when a tile exceeds it by more
 // than 2^8 (lazy rescale of the TMEM accumulator); the final normalisation
-// makes the result exact either way.  With several splits per token,
-// unnormalised partials (O, m, l) go to the workspace and a combine kernel
-// merges them.
+// makes the result exact either way.  With several splits per token, each
+// split's unnormalised output O (rounded to bf16, which keeps float32's
+// exponent range) and its (m, l) in float32 go to the workspace, and a
+// combine kernel merges them.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 
@@ -66,7 +67,7 @@ struct AttnParams {
     const int32_t *idx;
     float *out;
     float *lse;
-    float *part_o;           // [T, n_split, groups, 64, 512]
+    uint16_t *part_o;        // [T, n_split, groups, 64, 512] bf16, unnormalised
     float *part_ml;          // [T, n_split, groups, 64, 2]
     DevBatch b;
     uint32_t *status;
@@ -93,6 +94,7 @@ struct Ctl {
     float2 ma[kHeads];       // (m, alpha) of the current tile, read together
     int32_t resc[2];         // any head of warp 0 / 1 rescaled in this tile
     float l[kHeads];
+    float inv_l[kHeads];     // 1 / l (0 for an empty row)
     int32_t warp_alive[4];
 };
 
@@ -184,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!pos_ok && threadIdx.x == 0 && split == 0) flag(p.status, DSA_DEV_BAD_POSITION);
         // Empty contribution.
         if (p.n_split > 1) {
-            for (int i = threadIdx.x; i < kHeads * D_L; i += kThreads) p.part_o[part * kHeads * D_L + i] = 0.f;
+            for (int i = threadIdx.x; i < kHeads * D_L / 2; i += kThreads)
+                reinterpret_cast<uint32_t *>(p.part_o + part * kHeads * D_L)[i] = 0u;
             if (threadIdx.x < kHeads) {
                 float *ml = p.part_ml + (part * kHeads + threadIdx.x) * 2;
                 ml[0] = -INFINITY;
@@ -504,37 +507,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctl.red[sw][2 * lane] = l0;
         ctl.red[sw][2 * lane + 1] = l1;
         named_barrier(1, 128);
-        if (tx < kHeads) ctl.l[tx] = ctl.red[0][tx] + ctl.red[1][tx] + ctl.red[2][tx] + ctl.red[3][tx];
+        if (tx < kHeads) {
+            const float l = ctl.red[0][tx] + ctl.red[1][tx] + ctl.red[2][tx] + ctl.red[3][tx];
+            ctl.l[tx] = l;
+            ctl.inv_l[tx] = l > 0.f ? 1.f / l : 0.f;
+        }
         if (lane == 0) ctl.warp_alive[sw] = alive ? 1 : 0;
         named_barrier(1, 128);
         const bool all_alive = ctl.warp_alive[0] && ctl.warp_alive[1] && ctl.warp_alive[2] && ctl.warp_alive[3];
         if (all_alive) {
             // This CTA's [head][dim] block straight from TMEM: thread (quarter,
             // lane) holds output dim c*128 + quarter*32 + lane of every head,
-            // so each store instruction of a warp writes 128 contiguous bytes.
-            // Unnormalised partials when the token is split, the normalised
-            // output otherwise.
+            // so each warp store writes one head's contiguous run of dims.  The
+            // output (one split) is normalised and float32; a split's partial
+            // is unnormalised bf16 (measured on GB300, batched decode: the
+            // per-element 1 / l multiply there cost 3.6 us per CTA, pairing
+            // lanes for 4-byte stores 0.9 us).
             tc_fence_after();
             const int H = p.H;
-            const int rows = p.n_split > 1 ? kHeads : nh;
-            float *dst = p.n_split > 1 ? p.part_o + part * kHeads * D_L : p.out + ((int64_t)t * H + h0) * D_L;
             const int rd = quarter * 32 + lane;
-            for (int c = 0; c < 4; ++c) {
-                const int d = c * 128 + rd;
+            if (p.n_split == 1) {
+                // 16 heads at a time: their 1 / l in registers, then the 16
+                // accumulator columns of each 128-dim block
+                float *dst = p.out + ((int64_t)t * H + h0) * D_L;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float inv[16];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t u[32];
-                    tmem_ld32(tmem + lane_addr + kColO + c * kHeads + half * 32, u);
-                    tmem_wait_ld();
+                    for (int jj = 0; jj < 16; ++jj) inv[jj] = ctl.inv_l[q * 16 + jj];
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t u[16];
+                        tmem_ld16(tmem + lane_addr + kColO + c * kHeads + q * 16, u);
+                        tmem_wait_ld();
+                        const int d = c * 128 + rd;
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int h = half * 32 + jj;
-                        float o = __uint_as_float(u[jj]);
-                        if (p.n_split == 1) {
-                            const float l = ctl.l[h];
-                            o = l > 0.f ? o / l : 0.f;
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int h = q * 16 + jj;
+                            if (h < nh) dst[h * D_L + d] = __uint_as_float(u[jj]) * inv[jj];
                         }
-                        if (h < rows) dst[h * D_L + d] = o;
+                    }
+                }
+            } else {
+                uint16_t *dst = p.part_o + part * kHeads * D_L;
+                for (int c = 0; c < 4; ++c) {
+                    const int d = c * 128 + rd;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t u[32];
+                        tmem_ld32(tmem + lane_addr + kColO + c * kHeads + half * 32, u);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            dst[(half * 32 + jj) * D_L + d] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[jj])));
                     }
                 }
             }
@@ -565,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge split partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const float *__restrict__ part_o,
+__global__ void __launch_bounds__(128) attn_combine_kernel(const uint16_t *__restrict__ part_o,
                                                            const float *__restrict__ part_ml,
                                                            int n_split, int H, int groups, float *out, float *lse,
                                                            unsigned long long *timeline) {
@@ -594,17 +619,18 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float *__restri
     __syncthreads();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < n_split; s0 += 16) {              // 16 loads in flight
-        float4 o[16];
+        uint2 o[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u)
             if (s0 + u < n_split)
-                o[u] = __ldg(reinterpret_cast<const float4 *>(part_o + (base + (s0 + u) * stride) * D_L) +
-                             threadIdx.x);
+                o[u] = __ldg(reinterpret_cast<const uint2 *>(part_o + (base + (s0 + u) * stride) * D_L) + threadIdx.x);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             if (s0 + u < n_split) {
                 const float w = wgt[s0 + u];
-                acc.x += w * o[u].x; acc.y += w * o[u].y; acc.z += w * o[u].z; acc.w += w * o[u].w;
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&o[u].x));
+                const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&o[u].y));
+                acc.x += w * a.x; acc.y += w * a.y; acc.z += w * c.x; acc.w += w * c.y;
             }
         }
     }
@@ -629,7 +655,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch &a, const CUtensorMap &q_lat_map
     p.idx = a.idx;
     p.out = a.out;
     p.lse = a.lse;
-    p.part_o = a.part_o;
+    p.part_o = static_cast<uint16_t *>(a.part_o);
     p.part_ml = a.part_ml;
     p.b = b;
     p.status = status;
@@ -658,7 +684,7 @@ cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStre
     if (a.n_split > 128) return cudaErrorInvalidConfiguration;
     const int groups = (a.H + kHeads - 1) / kHeads;
     dim3 grid((unsigned)b.T, (unsigned)a.H);
-    return launch_k(attn_combine_kernel, grid, dim3(128), 0, stream, pdl, (const float *)a.part_o,
+    return launch_k(attn_combine_kernel, grid, dim3(128), 0, stream, pdl, (const uint16_t *)a.part_o,
                     (const float *)a.part_ml, a.n_split, a.H, groups, a.out, a.lse, b.timeline);
 }
 

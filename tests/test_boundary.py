@@ -90,11 +90,12 @@ def test_workspace_sizes(L):
 def test_split_partials_stay_within_what_the_combine_merges(L):
     """One token with k = 65536 (1024 row tiles) would ask for 147 splits;
     the layout caps them at the 128 the combine kernel merges, so the
-    workspace holds exactly 128 partials of 64 heads (plus their (m, l))."""
+    workspace holds exactly 128 bf16 partials of 64 heads (plus their (m, l)
+    in float32)."""
     n = C.c_size_t()
     b = _batch(batch=1, total_q=1, max_kv=70000, cache_rows=70000)
     assert L.dsa_workspace_size(dsa.DSA_OP_SPARSE_ATTN, C.byref(b), 4, 8, 65536, C.byref(n)) == dsa.DSA_OK
-    part_o, part_ml = 128 * 64 * 512 * 4, 128 * 64 * 2 * 4
+    part_o, part_ml = 128 * 64 * 512 * 2, 128 * 64 * 2 * 4
     assert n.value == 256 + part_o + part_ml
 
 
@@ -105,7 +106,7 @@ def test_head_groups_size_the_partials(L):
     b = _batch(batch=8, total_q=8, max_kv=8192, cache_rows=8 * 8192)
     assert L.dsa_workspace_size(dsa.DSA_OP_SPARSE_ATTN, C.byref(b), 64, 128, 2048, C.byref(n)) == dsa.DSA_OK
     rows = 8 * 8 * 2 * 64
-    assert n.value == 256 + rows * 512 * 4 + rows * 2 * 4
+    assert n.value == 256 + rows * 512 * 2 + rows * 2 * 4
     assert L.dsa_workspace_size(dsa.DSA_OP_SPARSE_ATTN, C.byref(b), 64, 129, 2048, C.byref(n)) == \
         dsa.DSA_ERR_UNSUPPORTED
 
