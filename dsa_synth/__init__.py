@@ -44,6 +44,9 @@ TID_W_UK = 9
 TID_W_UV = 10
 TID_Q_NOPE = 11
 TID_SCORES = 12
+TID_GATE_CACHE = 13
+TID_GATE_NEW = 14
+TID_APE = 15
 
 
 def splitmix64(x: np.ndarray) -> np.ndarray:
@@ -283,3 +286,63 @@ def batch_arrays(wl: Workload):
     return (np.asarray(wl.cu_q, dtype=np.int32),
             np.asarray(wl.q_pos, dtype=np.int32),
             np.asarray(wl.kv_off, dtype=np.int64))
+
+
+# ---------------------------------------------------------------------------
+# kpool indexer inputs (GLM-5.3-Flash DSA layers: MLA-NoPE latent rows of 512
+# and packed indexer rows of 257 fp16 values, k | gate | valid)
+# ---------------------------------------------------------------------------
+
+KPOOL_ROW = 257
+
+
+@dataclass
+class KpoolInputs:
+    """Host arrays of a kpool workload.
+
+    rows      float16 [rows, 257]   packed indexer rows: k (N(0,1)/sqrt(128)) |
+                                    gate (N(0,1)) | valid (1.0); the query
+                                    tokens' own rows hold stale draws until
+                                    the append writes them
+    k_new     float16 [T, 128]      new indexer keys
+    gate_new  float16 [T, 128]      new gate values
+    ape       float32 [4, 128]      position-in-pool embedding, N(0,1)
+    q_idx     float16 [T, H_I, 128] indexer queries
+    w         float32 [T, H_I]      per-head indexer weights
+    q_lat     uint16  [T, H, 512]   bf16 bits, latent queries
+    kv_latent uint16  [rows, 512]   bf16 bits, latent rows (no rope tail)
+    """
+    rows: np.ndarray
+    k_new: np.ndarray
+    gate_new: np.ndarray
+    ape: np.ndarray
+    q_idx: np.ndarray
+    w: np.ndarray
+    q_lat: np.ndarray
+    kv_latent: np.ndarray
+
+
+def pack_kpool_rows(k: np.ndarray, gate: np.ndarray, valid=None) -> np.ndarray:
+    """The packed row layout: k (128) | gate (128) | valid (1) as fp16."""
+    n = k.shape[0]
+    rows = np.empty((n, KPOOL_ROW), np.float16)
+    rows[:, :D_I] = k
+    rows[:, D_I:2 * D_I] = gate
+    rows[:, 2 * D_I] = 1.0 if valid is None else valid
+    return rows
+
+
+def make_kpool_inputs(wl: Workload) -> KpoolInputs:
+    s = wl.seed
+    rows, T = wl.cache_rows, wl.T
+    k = normal(s, TID_K_CACHE, (rows, D_I), 1 / math.sqrt(D_I), "f16")
+    g = normal(s, TID_GATE_CACHE, (rows, D_I), 1.0, "f16")
+    return KpoolInputs(
+        rows=pack_kpool_rows(k, g),
+        k_new=normal(s, TID_K_NEW, (T, D_I), 1 / math.sqrt(D_I), "f16"),
+        gate_new=normal(s, TID_GATE_NEW, (T, D_I), 1.0, "f16"),
+        ape=normal(s, TID_APE, (4, D_I), 1.0, "f32"),
+        q_idx=normal(s, TID_Q_IDX, (T, wl.H_I, D_I), 1 / math.sqrt(D_I), "f16"),
+        w=normal(s, TID_W, (T, wl.H_I), 1 / math.sqrt(wl.H_I), "f32"),
+        q_lat=normal(s, TID_Q_LAT, (T, wl.H, D_L), 1 / math.sqrt(D_L), "bf16"),
+        kv_latent=normal(s, TID_KV_CACHE, (rows, D_L), 1 / math.sqrt(D_L), "bf16"))

@@ -44,6 +44,9 @@ def lib():
             "oracle_decode": (I32, [P, I32, P, P, P, P, P, P, I32, I32, P, P, P, I32, I32, I32, F64,
                                     I32, P, I64, P, P, P]),
             "oracle_set_threads": (I32, [I32]),
+            "oracle_kpool_write_rows": (I32, [P, P, I32, I32, P, P, P, P]),
+            "oracle_kpool_pool_key": (I32, [P, I64, P, P]),
+            "oracle_kpool_select": (I32, [P, P, P, P, I32, I32, P, P, P, I32, I32, P, P, I64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -266,3 +269,46 @@ def decode(inp, wl, k_cache=None, ld: int | None = None):
                                wl.H_I, wl.H, wl.top_k, wl.sm_scale, int(wl.hadamard),
                                _p(scores), ld, _p(idx), _p(out), _p(lse)), "decode")
     return dict(k_cache=kc, scores=scores, idx=idx, out=out, lse=lse)
+
+
+# ---------------------------------------------------------------- kpool indexer
+# GLM-5.3-Flash (vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on gfx1030"): the
+# reading is stated in dsa_oracle.h.
+
+KPOOL = 4
+KPOOL_ROW = 257
+
+
+def kpool_width(top_k: int) -> int:
+    """Index entries per token: floor(top_k / 4) pools of 4 positions plus a
+    tail of at most 3 (2051 for top_k = 2048)."""
+    return (top_k // KPOOL) * KPOOL + KPOOL - 1
+
+
+def kpool_write_rows(k_new, gate_new, batch: Batch, rows: np.ndarray) -> None:
+    """Packed rows k|gate|1.0 (fp16, [rows, 257]) of the new tokens, in place."""
+    assert rows.dtype == np.float16 and rows.flags.c_contiguous and rows.shape[1] == KPOOL_ROW
+    _check(lib().oracle_kpool_write_rows(_p(_c(k_new, np.float16)), _p(_c(gate_new, np.float16)), *batch.args(),
+                                         _p(rows)), "kpool_write_rows")
+
+
+def kpool_pool_key(seq_rows, j: int, ape):
+    """(has_key, key fp16 [128]) of pool j of a sequence's packed rows."""
+    r = _c(seq_rows, np.float16)
+    key = np.zeros(128, np.float16)
+    has = lib().oracle_kpool_pool_key(_p(r), int(j), _p(_c(ape, np.float32)), _p(key))
+    return bool(has), key
+
+
+def kpool_select(q_idx, w, rows, ape, batch: Batch, top_k: int, scores: bool = False):
+    """Token positions [T, kpool_width(top_k)] (and, with scores, the pool
+    scores [T, max pools])."""
+    q = _c(q_idx, np.float16)
+    T, H_I, _ = q.shape
+    width = kpool_width(top_k)
+    idx = np.empty((T, width), np.int32)
+    ld = int(max(1, (int(batch.q_pos.max()) + 1) // KPOOL)) if T else 1
+    sc = np.empty((T, ld), np.float64) if scores else None
+    _check(lib().oracle_kpool_select(_p(q), _p(_c(w, np.float32)), _p(_c(rows, np.float16)), _p(_c(ape, np.float32)),
+                                     *batch.args(), H_I, top_k, _p(idx), _p(sc), ld), "kpool_select")
+    return (idx, sc) if scores else idx

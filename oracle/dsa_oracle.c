@@ -505,3 +505,113 @@ int oracle_decode(const void *k_new, int k_dtype, const uint16_t *q_idx, const f
                                      k, H, sm_scale, out, lse);
     return rc;
 }
+
+/* ---------------------------------------------------------------- kpool indexer */
+
+int oracle_kpool_write_rows(const uint16_t *k_new, const uint16_t *gate_new, int B, int T,
+                            const int32_t *cu_q, const int32_t *q_pos, const int64_t *kv_off,
+                            uint16_t *rows)
+{
+    if (check_batch(B, T, cu_q, q_pos)) return -1;
+    for (int t = 0; t < T; t++) {
+        int b = seq_of(t, B, cu_q);
+        uint16_t *r = rows + (kv_off[b] + q_pos[t]) * (int64_t)ORACLE_KPOOL_ROW;
+        for (int d = 0; d < D_I; d++) {
+            r[d] = k_new[(int64_t)t * D_I + d];
+            r[D_I + d] = gate_new[(int64_t)t * D_I + d];
+        }
+        r[2 * D_I] = 0x3C00;                               /* valid = 1.0 */
+    }
+    return 0;
+}
+
+static int row_valid(const uint16_t *r) { return oracle_f16_to_f64(r[2 * D_I]) != 0.0; }
+
+int oracle_kpool_pool_key(const uint16_t *seq_rows, int64_t j, const float *ape, uint16_t *key)
+{
+    const uint16_t *r[ORACLE_KPOOL];
+    int any = 0;
+    for (int i = 0; i < ORACLE_KPOOL; i++) {
+        r[i] = seq_rows + (j * ORACLE_KPOOL + i) * (int64_t)ORACLE_KPOOL_ROW;
+        any |= row_valid(r[i]);
+    }
+    if (!any) return 0;
+    for (int d = 0; d < D_I; d++) {
+        /* softmax over the valid positions of (gate + ape), max-subtracted */
+        double e[ORACLE_KPOOL], m = -INFINITY;
+        for (int i = 0; i < ORACLE_KPOOL; i++) {
+            e[i] = oracle_f16_to_f64(r[i][D_I + d]) + (double)ape[i * D_I + d];
+            if (row_valid(r[i]) && e[i] > m) m = e[i];
+        }
+        double den = 0.0, num = 0.0;
+        for (int i = 0; i < ORACLE_KPOOL; i++) {
+            if (!row_valid(r[i])) continue;
+            double a = exp(e[i] - m);
+            den += a;
+            num += a * oracle_f16_to_f64(r[i][d]);
+        }
+        key[d] = oracle_f64_to_f16(num / den);
+    }
+    return 1;
+}
+
+int oracle_kpool_select(const uint16_t *q_idx, const float *w, const uint16_t *rows, const float *ape,
+                        int B, int T, const int32_t *cu_q, const int32_t *q_pos, const int64_t *kv_off,
+                        int H_I, int top_k, int32_t *idx, double *pool_scores, int64_t ld_pools)
+{
+    if (check_batch(B, T, cu_q, q_pos) || H_I < 1 || top_k < 1) return -1;
+    const int kp = top_k / ORACLE_KPOOL;                   /* pools selected */
+    const int width = kp * ORACLE_KPOOL + ORACLE_KPOOL - 1;
+    for (int t = 0; t < T; t++)
+        if (pool_scores && (q_pos[t] + 1) / ORACLE_KPOOL > ld_pools) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; t++) {
+        const int b = seq_of(t, B, cu_q);
+        const int p = q_pos[t];
+        const int n_pools = (p + 1) / ORACLE_KPOOL;        /* complete pools visible */
+        const uint16_t *seq_rows = rows + kv_off[b] * (int64_t)ORACLE_KPOOL_ROW;
+        cand_t *c = malloc(sizeof(cand_t) * (size_t)(n_pools > 0 ? n_pools : 1));
+        uint16_t *keys = malloc(sizeof(uint16_t) * (size_t)(n_pools > 0 ? n_pools : 1) * D_I);
+        if (!c || !keys) { bad = 1; free(c); free(keys); continue; }
+        if (pool_scores)
+            for (int64_t j = 0; j < ld_pools; j++) pool_scores[(int64_t)t * ld_pools + j] = -INFINITY;
+        int n_c = 0;
+        for (int j = 0; j < n_pools; j++) {
+            uint16_t *key = keys + (size_t)j * D_I;
+            if (!oracle_kpool_pool_key(seq_rows, j, ape, key)) continue;
+            double I = 0.0;
+            for (int h = 0; h < H_I; h++) {
+                double dot = 0.0;
+                for (int d = 0; d < D_I; d++)
+                    dot += oracle_f16_to_f64(q_idx[((int64_t)t * H_I + h) * D_I + d]) * oracle_f16_to_f64(key[d]);
+                I += (double)w[(int64_t)t * H_I + h] * (dot > 0.0 ? dot : 0.0);
+            }
+            if (pool_scores) pool_scores[(int64_t)t * ld_pools + j] = I;
+            c[n_c].v = I;
+            c[n_c].s = j;
+            n_c++;
+        }
+        /* the best floor(top_k / 4) pools by (score desc, pool asc), in pool order */
+        qsort(c, (size_t)n_c, sizeof(cand_t), by_score_desc_pos_asc);
+        int m = n_c < kp ? n_c : kp;
+        int32_t *sel = malloc(sizeof(int32_t) * (size_t)(m > 0 ? m : 1));
+        if (!sel) { bad = 1; free(c); free(keys); continue; }
+        for (int i = 0; i < m; i++) sel[i] = c[i].s;
+        qsort(sel, (size_t)m, sizeof(int32_t), by_pos);
+        int32_t *out = idx + (int64_t)t * width;
+        int n = 0;
+        for (int i = 0; i < m; i++)                        /* each pool's valid positions */
+            for (int r = 0; r < ORACLE_KPOOL; r++) {
+                const int s = sel[i] * ORACLE_KPOOL + r;
+                if (row_valid(seq_rows + (int64_t)s * ORACLE_KPOOL_ROW)) out[n++] = s;
+            }
+        for (int s = n_pools * ORACLE_KPOOL; s <= p; s++)  /* the tail, always */
+            if (row_valid(seq_rows + (int64_t)s * ORACLE_KPOOL_ROW)) out[n++] = s;
+        for (; n < width; n++) out[n] = -1;
+        free(sel);
+        free(c);
+        free(keys);
+    }
+    return bad ? -1 : 0;
+}

@@ -140,4 +140,46 @@ int oracle_set_threads(int n);
 #ifdef __cplusplus
 }
 #endif
+/* ---------------------------------------------------------------- kpool indexer
+ * GLM-5.3-Flash (vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on gfx1030", the
+ * DSA layer bullet): a kpool indexer (32 heads x 128, topk 2048, kpool 4,
+ * always_select_tail, pool compression softmax(gate+ape), tail <= 3 ->
+ * width 2051) whose cache holds packed indexer rows of 257 fp16 values,
+ * k (128) | gate (128) | valid (1).  Reading taken (the page gives only this
+ * outline):
+ *  - pools are the aligned runs of 4 positions [4j, 4j+4) of a sequence; a
+ *    pool is visible to a query at position p when 4j + 3 <= p; the tail is
+ *    the positions 4*floor((p+1)/4) .. p (at most 3);
+ *  - the pooled key of pool j, per dim d: softmax over the pool's valid rows
+ *    i of (gate[4j+i][d] + ape[i][d]) weighting k[4j+i][d], rounded once to
+ *    fp16 (ape: [4][128] position-in-pool embedding, a model parameter);
+ *    a pool with no valid row has no key;
+ *  - pool scores follow the indexer formula on the pooled keys (no rotation,
+ *    no extra scale constant);
+ *  - top_k counts tokens: the floor(top_k / 4) best pools by (score desc,
+ *    pool asc) are expanded to their valid positions, the valid tail
+ *    positions are always added, the list is ascending and padded with -1 to
+ *    width 4*floor(top_k/4) + 3 (2051 for top_k = 2048).
+ */
+#define ORACLE_KPOOL 4
+#define ORACLE_KPOOL_ROW 257
+
+/* Packed rows k|gate|1.0 of the new tokens at kv_off[b] + q_pos[t]. */
+int oracle_kpool_write_rows(const uint16_t *k_new, const uint16_t *gate_new, int B, int T,
+                            const int32_t *cu_q, const int32_t *q_pos, const int64_t *kv_off,
+                            uint16_t *rows);
+
+/* Pooled key of pool j of the sequence whose packed rows start at seq_rows.
+ * Returns 1 and writes key[128] (fp16 bits) when the pool has a valid row,
+ * else returns 0 and leaves key untouched. */
+int oracle_kpool_pool_key(const uint16_t *seq_rows, int64_t j, const float *ape, uint16_t *key);
+
+/* Selection of every query token: idx [T, width] token positions (ascending,
+ * -1 padded), width = 4*floor(top_k/4) + 3.  pool_scores (nullable)
+ * [T, ld_pools] receives the pool scores (-inf for pools not visible or
+ * without a key). */
+int oracle_kpool_select(const uint16_t *q_idx, const float *w, const uint16_t *rows, const float *ape,
+                        int B, int T, const int32_t *cu_q, const int32_t *q_pos, const int64_t *kv_off,
+                        int H_I, int top_k, int32_t *idx, double *pool_scores, int64_t ld_pools);
+
 #endif
