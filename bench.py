@@ -42,7 +42,7 @@ sys.path.insert(0, ROOT)
 METRIC = "DSA decode tok/s & prefill tok/s on 1 GB300; % of HBM / tensor roofline"
 UNIT = "tok/s"
 WORKLOADS = {"tiny_decode": 1, "batched_decode": 2, "ragged_decode": 3, "prefill_chunk": 4, "long_prefill": 5,
-             "indexshare_decode": 2}
+             "indexshare_decode": 2, "kpool_decode": 2}
 STACK_LAYERS = 78
 MAX_TRACE_WINDOWS = 32    # score windows whose top-k launch the trace events bracket
 
@@ -513,7 +513,7 @@ def layer_stack(args):
 # ---------------------------------------------------------------------------- GPU arm
 
 TIMELINE_ORDER = ["k_append", "indexer_score", "topk", "sparse_attn", "attn_combine"]
-EXTRA_WORKLOADS = ["ragged_decode", "prefill_chunk", "long_prefill"]
+EXTRA_WORKLOADS = ["ragged_decode", "prefill_chunk", "long_prefill", "kpool_decode"]
 
 
 def exclusive_spans(spans):
@@ -732,13 +732,15 @@ def score_windows(dsa, batch):
     return (n - append - 1) // 2
 
 
-def workload_line(wl, res, pk, steps, headline=False):
+def workload_line(wl, res, pk, steps, headline=False, alg=None):
     """The numbers of one workload: throughput, per-kernel rooflines, the
     dominant kernel (longest per-kernel time) and the whole step against the
     HBM roofline of the bytes it must move."""
-    alg = algorithmic(wl)
+    alg = alg or algorithmic(wl)
     ms = statistics.fmean(res["step_ms"])
     kernels = {st: dict(ms=round(m, 5), **kernel_roofline(st, m, wl, alg, pk)) for st, m in res["kernel_ms"].items()}
+    if alg.get("kpool"):
+        kernels.get("k_append", {})["kernel_name"] = "kpool_append_kernel"
     dom = max(res["kernel_ms"], key=res["kernel_ms"].get)
     roof = dict(kernels[dom])
     roof["kernel"] = KERNEL_OF_STAGE[dom]
@@ -755,6 +757,129 @@ def workload_line(wl, res, pk, steps, headline=False):
             "timeline_us": res["timeline_us"], "stages_ms": res["stages_ms"], "clocks": res["clocks"],
             "gpu_launches_per_step": res["launches"]}
     return line
+
+
+def kpool_workload():
+    """GLM-5.3-Flash DSA decode (vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash) on
+    gfx1030": kpool indexer 32 heads x 128, top_k 2048 -> 2051 positions,
+    MLA-NoPE attention on 512-d latents, 64 heads): 8 sequences of 8192
+    positions, the batched-decode shapes without the rope tail."""
+    import dsa_synth as S
+    return S.Workload("kpool_decode_B8_L8192", 6, kv_len=[8192] * 8, q_pos=[8191] * 8, cu_q=list(range(9)),
+                      H_I=32, H=64, top_k=2048)
+
+
+def kpool_algorithmic(wl):
+    """Bytes a kpool decode step must move: every visible pooled key of each
+    sequence (256 B per pool) and each token's selected latent rows (1024 B
+    each, at most 4 floor(top_k/4) + 3); flops of the pool scores and the
+    attention."""
+    pools = sum((p + 1) // 4 for p in wl.q_pos)
+    width = (wl.top_k // 4) * 4 + 3
+    sel = sum(min(width, p + 1) for p in wl.q_pos)
+    return dict(score_bytes=pools * 256, attn_bytes=sel * 1024, step_bytes=pools * 256 + sel * 1024,
+                score_flops=pools * wl.H_I * 256, attn_flops=sel * wl.H * 2 * (512 + 512),
+                topk_bytes=pools * 4, append_bytes=wl.T * 2 * 514, out_bytes=wl.T * wl.H * 512 * 4)
+
+
+def measure_kpool(dsa, torch, wl, steps, warmup, flush_mb, world=1):
+    """dsa_decode_kpool steps, timed like measure(): the context's pooled keys
+    are built first by appending every cached position."""
+    import numpy as np
+    import dsa_synth as S
+    inp = S.make_kpool_inputs(wl)
+
+    def up(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    rows, kv_latent = up(inp.rows), up(inp.kv_latent)
+    pool = torch.zeros(((wl.cache_rows + 3) // 4, 128), dtype=torch.float16, device="cuda")
+    ape = up(inp.ape)
+    # context: positions 0 .. p - 1 of every sequence, with the rows' own k and gate
+    ctx_pos = [s for p in wl.q_pos for s in range(p)]
+    ctx_cu = [0]
+    for p in wl.q_pos:
+        ctx_cu.append(ctx_cu[-1] + p)
+    tok = [wl.kv_off[b] + s for b, p in enumerate(wl.q_pos) for s in range(p)]
+    b_ctx = dsa.Batch.from_host(ctx_cu, ctx_pos, wl.kv_off, wl.cache_rows, max_q_per_seq=max(wl.q_pos),
+                                max_kv=max(wl.q_pos))
+    ws0 = dsa.workspace(dsa.DSA_OP_K_APPEND, b_ctx)
+    dsa.dsa_kpool_append(up(np.ascontiguousarray(inp.rows[tok, :128])), up(np.ascontiguousarray(inp.rows[tok, 128:256])),
+                         ape, b_ctx, rows, pool, ws0)
+    torch.cuda.synchronize()
+    batch = dsa.Batch.from_host(wl.cu_q, wl.q_pos, wl.kv_off, wl.cache_rows, max_q_per_seq=wl.max_q_per_seq,
+                                max_kv=wl.max_kv)
+    ws = dsa.workspace(dsa.DSA_OP_KPOOL, batch, wl.H_I, wl.H, wl.top_k)
+    k_new, gate_new, q_idx, w, q_lat = (up(inp.k_new), up(inp.gate_new), up(inp.q_idx), up(inp.w), up(inp.q_lat))
+    out = torch.empty((wl.T, wl.H, 512), device="cuda")
+    lse = torch.empty((wl.T, wl.H), device="cuda")
+    idx = torch.empty((wl.T, dsa.kpool_width(wl.top_k)), dtype=torch.int32, device="cuda")
+    flush = torch.empty(flush_mb << 20, dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones((flush_mb << 20) // 4, dtype=torch.float32, device="cuda")
+    tl_buf = torch.zeros(10, dtype=torch.int64, device="cuda")
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        flush_r.amax()
+
+    def step():
+        dsa.dsa_decode_kpool(k_new, gate_new, ape, q_idx, w, q_lat, rows, pool, kv_latent, batch, wl.top_k,
+                             wl.sm_scale, out, lse, idx, ws)
+
+    for i in range(3 + warmup):
+        flush_l2(i)
+        step()
+    torch.cuda.synchronize()
+    if dsa.dsa_read_device_status(ws) != 0:
+        raise RuntimeError(f"{wl.name}: device status flags set during warm-up")
+    clocks = Clocks(gpu_index_for(torch.cuda.current_device()))
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(i)
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_rows = clocks.stop()
+    big = torch.iinfo(torch.int64).max
+    excl = {st: [] for st in TIMELINE_ORDER}
+    spans = {st: [] for st in TIMELINE_ORDER}
+    for i in range(min(steps, 200)):
+        tl_buf[0::2] = big
+        tl_buf[1::2] = 0
+        flush_l2(i)
+        dsa.dsa_set_timeline(tl_buf)
+        step()
+        dsa.dsa_set_timeline(None)
+        torch.cuda.synchronize()
+        v = tl_buf.tolist()
+        t0 = min(x for x in v[0::2] if x != big)
+        sp = {st: ((v[2 * j] - t0) / 1e3, (v[2 * j + 1] - t0) / 1e3)
+              for j, st in enumerate(TIMELINE_ORDER) if v[2 * j] != big}
+        for st, x in sp.items():
+            spans[st].append(x)
+        for st, x in exclusive_spans(sp).items():
+            excl[st].append(x)
+    if dsa.dsa_read_device_status(ws) != 0:
+        raise RuntimeError(f"{wl.name}: device status flags set during the timed steps")
+    # 2 appends? one (one token per sequence); then a score and top-k per
+    # window, the expansion, the attention and (split tokens) the combine
+    return dict(step_ms=[a.elapsed_time(b) for a, b in ev],
+                kernel_ms={st: statistics.median(v) / 1e3 for st, v in excl.items() if v},
+                kernel_source=("device timeline (globaltimer): exclusive spans in the overlapped step (the expansion "
+                               "kernel between top-k and attention has no slot and falls in the attention's share)"),
+                launches=6, clocks=Clocks.summary(clock_rows),
+                timeline_us={st: [round(statistics.median(a for a, _ in v), 2),
+                                  round(statistics.median(b for _, b in v), 2)] for st, v in spans.items() if v},
+                stages_ms={})
 
 
 def main():
@@ -785,6 +910,16 @@ def main():
     import dsa_synth as S
 
     pk = peaks()
+    if args.workload == "kpool_decode":                  # the GLM-5.3-Flash step alone
+        w2 = kpool_workload()
+        r2 = measure_kpool(dsa, torch, w2, args.steps, args.warmup, args.flush_mb, world=world)
+        line = workload_line(w2, r2, pk, args.steps, alg=dict(kpool_algorithmic(w2), kpool=True))
+        line.update(metric=METRIC, unit=UNIT, value=job_throughput(world, w2.T, args.steps,
+                                                                       max_over_ranks(sum(r2["step_ms"]) / 1e3)),
+                    n_gpus=world, higher_is_better=True, scaling="weak", config={"workload": w2.name})
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
     wl = S.config(WORKLOADS[args.workload])
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     res = measure(dsa, torch, wl, args.steps, args.warmup, args.flush_mb, world=world, e2e_steps=n_e2e,
@@ -803,10 +938,16 @@ def main():
     if not args.headline_only and args.workload == "batched_decode":
         for name in EXTRA_WORKLOADS:
             torch.cuda.empty_cache()
-            w2 = S.config(WORKLOADS[name])
             n2 = max(3, min(args.steps, 20 if name != "long_prefill" else 10))
-            r2 = measure(dsa, torch, w2, n2, max(3, min(args.warmup, 5)), args.flush_mb, world=world)
-            extra[name] = workload_line(w2, r2, pk, n2)
+            if name == "kpool_decode":
+                w2 = kpool_workload()
+                r2 = measure_kpool(dsa, torch, w2, n2, max(3, min(args.warmup, 5)), args.flush_mb, world=world)
+                extra[name] = workload_line(w2, r2, pk, n2, alg=dict(kpool_algorithmic(w2), kpool=True))
+                extra[name]["selection_width"] = dsa.kpool_width(w2.top_k)
+            else:
+                w2 = S.config(WORKLOADS[name])
+                r2 = measure(dsa, torch, w2, n2, max(3, min(args.warmup, 5)), args.flush_mb, world=world)
+                extra[name] = workload_line(w2, r2, pk, n2)
             extra[name]["ms_per_step"] = 1e3 * max_over_ranks(sum(r2["step_ms"]) / 1e3) / n2
             extra[name]["tok_s"] = job_throughput(world, w2.T, n2, 1e-3 * extra[name]["ms_per_step"] * n2)
             gpu_launches += r2["launches"] * n2

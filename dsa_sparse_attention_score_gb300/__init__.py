@@ -39,6 +39,10 @@ DSA_OP_INDEXER_SCORE = 1
 DSA_OP_TOPK = 2
 DSA_OP_SPARSE_ATTN = 3
 DSA_OP_DECODE = 4
+DSA_OP_KPOOL = 5
+
+KPOOL = 4            # positions per pool of the kpool indexer
+KPOOL_ROW = 257      # fp16 values per packed indexer row: k | gate | valid
 
 # Every symbol the header declares, with (restype, argtypes).
 _P = C.c_void_p
@@ -76,6 +80,10 @@ SIGNATURES = {
     "dsa_set_trace_events": (_I, [_P, _I]),
     "dsa_set_timeline": (_I, [_P]),
     "dsa_set_test_faults": (_I, [C.c_uint64, _I]),
+    "dsa_kpool_append": (_I, [_P, _P, _P, _BP, _P, _P, _I64, _P, _SZ, _P]),
+    "dsa_kpool_select": (_I, [_P, _P, _P, _P, _I64, _BP, _I, _I, _P, _P, _SZ, _P]),
+    "dsa_decode_kpool": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _BP, _I, _I, _I, _F, _P, _P, _P, _P, _SZ,
+                              _P]),
     "dsa_version": (_I, []),
 }
 
@@ -119,7 +127,7 @@ def _stream(stream=None):
 
 
 # Fixed innermost extents of the tensors the calls take (include/dsa.h).
-_WIDTH = {"k_new": 128, "q_idx": 128, "k_cache": 128, "q_lat": 512, "q_rope": 64, "kv_cache": 576,
+_WIDTH = {"k_new": 128, "gate_new": 128, "ape": 128, "q_idx": 128, "k_cache": 128, "q_lat": 512, "q_rope": 64, "kv_cache": 576,
           "kv_latent": 512, "out": 512}
 
 
@@ -375,6 +383,70 @@ def dsa_decode_noalloc(k_new, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch:
                                     _ptr(k_cache), _ptr(kv_cache), C.byref(d), q_idx.shape[1], q_lat.shape[1], k,
                                     sm_scale, int(hadamard), _ptr(out), _ptr(lse), _ptr(idx_out),
                                     _stream(stream)), "dsa_decode_noalloc")
+
+
+def kpool_width(top_k: int) -> int:
+    """Positions per token of a kpool selection: 4 * floor(top_k / 4) + 3."""
+    return (top_k // KPOOL) * KPOOL + KPOOL - 1
+
+
+def _req_rows(rows):
+    import torch
+    if not rows.is_cuda or rows.dtype != torch.float16 or not rows.is_contiguous() or rows.dim() != 2 \
+            or rows.shape[1] != KPOOL_ROW:
+        raise TypeError(f"idx_rows: expected a contiguous CUDA float16 [rows, {KPOOL_ROW}] tensor")
+
+
+def dsa_kpool_append(k_new, gate_new, ape, batch: Batch, idx_rows, pool_keys, ws, stream=None):
+    """Packed rows k|gate|1.0 of the new tokens and the pooled key of every
+    pool they complete (GLM-5.3-Flash kpool indexer)."""
+    import torch
+    _req(k_new, torch.float16, "k_new")
+    _req(gate_new, torch.float16, "gate_new")
+    _req(ape, torch.float32, "ape")
+    _req_rows(idx_rows)
+    _req(pool_keys, torch.float16, "k_cache")
+    d = batch.desc()
+    _check(lib().dsa_kpool_append(_ptr(k_new), _ptr(gate_new), _ptr(ape), C.byref(d), _ptr(idx_rows),
+                                  _ptr(pool_keys), pool_keys.shape[0], _ptr(ws), ws.numel(), _stream(stream)),
+           "dsa_kpool_append")
+
+
+def dsa_kpool_select(q_idx, w, idx_rows, pool_keys, batch: Batch, top_k: int, idx, ws, stream=None):
+    """Positions [T, kpool_width(top_k)] of the best top_k/4 pools and the tail."""
+    import torch
+    _req(q_idx, torch.float16, "q_idx")
+    _req(w, torch.float32, "w")
+    _req_rows(idx_rows)
+    _req(pool_keys, torch.float16, "k_cache")
+    _req(idx, torch.int32, "idx")
+    d = batch.desc()
+    _check(lib().dsa_kpool_select(_ptr(q_idx), _ptr(w), _ptr(idx_rows), _ptr(pool_keys), pool_keys.shape[0],
+                                  C.byref(d), q_idx.shape[1], top_k, _ptr(idx), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "dsa_kpool_select")
+
+
+def dsa_decode_kpool(k_new, gate_new, ape, q_idx, w, q_lat, idx_rows, pool_keys, kv_latent, batch: Batch, top_k: int,
+                     sm_scale: float, out, lse, idx_out, ws, stream=None):
+    """The fused GLM-5.3-Flash DSA step: kpool append, selection, MLA-NoPE attention."""
+    import torch
+    _req(k_new, torch.float16, "k_new")
+    _req(gate_new, torch.float16, "gate_new")
+    _req(ape, torch.float32, "ape")
+    _req(q_idx, torch.float16, "q_idx")
+    _req(w, torch.float32, "w")
+    _req(q_lat, torch.bfloat16, "q_lat")
+    _req_rows(idx_rows)
+    _req(pool_keys, torch.float16, "k_cache")
+    _req(kv_latent, torch.bfloat16, "kv_latent")
+    _req(out, torch.float32, "out")
+    _req(lse, torch.float32, "lse")
+    _req(idx_out, torch.int32, "idx_out")
+    d = batch.desc()
+    _check(lib().dsa_decode_kpool(_ptr(k_new), _ptr(gate_new), _ptr(ape), _ptr(q_idx), _ptr(w), _ptr(q_lat),
+                                  _ptr(idx_rows), _ptr(pool_keys), pool_keys.shape[0], _ptr(kv_latent), C.byref(d),
+                                  q_idx.shape[1], q_lat.shape[1], top_k, sm_scale, _ptr(out), _ptr(lse),
+                                  _ptr(idx_out), _ptr(ws), ws.numel(), _stream(stream)), "dsa_decode_kpool")
 
 
 def dsa_set_trace_events(events):

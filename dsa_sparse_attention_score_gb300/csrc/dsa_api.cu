@@ -23,6 +23,7 @@ int g_skip_copies = 0;
 
 constexpr int kMaxHeads = 128;        // query heads: one or two groups of 64 per token
 constexpr int kMaxSplit = 128;        // split partials the combine kernel merges
+constexpr int kKpoolMaxTopK = 4096;   // kpool: 1024 pools per token (the expansion's slots)
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -54,6 +55,7 @@ DevBatch dev_batch(const dsa_batch_t *b) {
     d.block_size = 0;
     d.wait_ns = g_wait_ns;
     d.skip_copies = g_skip_copies;
+    d.pool_log2 = 0;
     return d;
 }
 
@@ -96,6 +98,7 @@ struct Layout {
     size_t status = 0;
     size_t scores = 0, scores_bytes = 0;
     size_t idx = 0, idx_bytes = 0;
+    size_t pool_idx = 0;      // kpool: selected pools [T, top_k / 4]
     size_t part_o = 0, part_o_bytes = 0;
     size_t part_ml = 0, part_ml_bytes = 0;
     size_t total = 0;
@@ -114,7 +117,7 @@ void attn_split(int T, int H, int k, int *n_split, int *tpc) {
     const int n_tiles = (k + attn_tile_rows() - 1) / attn_tile_rows();
     const int64_t units = (int64_t)T * head_groups(H);
     int ns = 1;
-    if (units < kSMs) ns = std::max(1, std::min(n_tiles / 2, (int)(kSMs / units)));
+    if (units < kSMs) ns = std::max(1, std::min((n_tiles + 1) / 2, (int)(kSMs / units)));
     ns = std::min(ns, kMaxSplit);
     int t = (n_tiles + ns - 1) / ns;
     ns = (n_tiles + t - 1) / t;
@@ -122,9 +125,31 @@ void attn_split(int T, int H, int k, int *n_split, int *tpc) {
     *tpc = t;
 }
 
+// kpool: pools selected per token and the width of a token's position list.
+inline int kpool_pools(int top_k) { return top_k / kKpool; }
+inline int kpool_width(int top_k) { return kpool_pools(top_k) * kKpool + kKpool - 1; }
+
 Layout layout(int op, const dsa_batch_t *b, int H, int k) {
     Layout L;
     size_t off = kStatusBytes;
+    if (op == DSA_OP_KPOOL) {
+        // score slab over pools, the selected pools, the expanded positions,
+        // then the attention's split partials over those positions
+        const int max_pools = std::max(1, b->max_kv / kKpool);
+        L.ld = (int64_t)align_up((size_t)max_pools, 4);
+        const int64_t row_bytes = L.ld * 4;
+        int64_t J = std::max<int64_t>(1, kSlabBytes / (row_bytes * b->batch));
+        L.J = (int)std::min<int64_t>(J, b->max_q_per_seq);
+        L.scores = off;
+        L.scores_bytes = (size_t)b->batch * L.J * row_bytes;
+        off = align_up(off + L.scores_bytes, kAlign);
+        L.pool_idx = off;
+        off = align_up(off + (size_t)b->total_q * std::max(1, kpool_pools(k)) * 4, kAlign);
+        L.idx = off;
+        L.idx_bytes = (size_t)b->total_q * kpool_width(k) * 4;
+        off = align_up(off + L.idx_bytes, kAlign);
+        k = kpool_width(k);                          // the attention runs over the positions
+    }
     if (op == DSA_OP_DECODE) {
         L.ld = (int64_t)align_up((size_t)b->max_kv, 4);
         const int64_t row_bytes = L.ld * 4;
@@ -137,7 +162,7 @@ Layout layout(int op, const dsa_batch_t *b, int H, int k) {
         L.idx_bytes = (size_t)b->total_q * k * 4;
         off = align_up(off + L.idx_bytes, kAlign);
     }
-    if (op == DSA_OP_DECODE || op == DSA_OP_SPARSE_ATTN) {
+    if (op == DSA_OP_DECODE || op == DSA_OP_SPARSE_ATTN || op == DSA_OP_KPOOL) {
         attn_split(b->total_q, H, k, &L.n_split, &L.tiles_per_cta);
         if (L.n_split > 1) {
             const size_t rows = (size_t)b->total_q * L.n_split * head_groups(H) * 64;
@@ -271,12 +296,14 @@ dsa_status_t dsa_set_test_faults(uint64_t wait_limit_ns, int skip_copies) {
 
 dsa_status_t dsa_workspace_size(int op, const dsa_batch_t *batch, int H_I, int H, int k, size_t *bytes) {
     (void)H_I;
-    if (!bytes || op < DSA_OP_K_APPEND || op > DSA_OP_DECODE) return DSA_ERR_INVALID_ARGUMENT;
+    if (!bytes || op < DSA_OP_K_APPEND || op > DSA_OP_KPOOL) return DSA_ERR_INVALID_ARGUMENT;
     if (!batch || batch->batch < 1 || batch->total_q < 1 || batch->max_q_per_seq < 1 || batch->max_kv < 1)
         return DSA_ERR_INVALID_ARGUMENT;
     if ((op == DSA_OP_TOPK || op == DSA_OP_SPARSE_ATTN || op == DSA_OP_DECODE) && (k < 1 || k > 65536))
         return DSA_ERR_UNSUPPORTED;
-    if ((op == DSA_OP_SPARSE_ATTN || op == DSA_OP_DECODE) && (H < 1 || H > kMaxHeads)) return DSA_ERR_UNSUPPORTED;
+    if (op == DSA_OP_KPOOL && (k < 1 || k > kKpoolMaxTopK)) return DSA_ERR_UNSUPPORTED;
+    if ((op == DSA_OP_SPARSE_ATTN || op == DSA_OP_DECODE || op == DSA_OP_KPOOL) && (H < 1 || H > kMaxHeads))
+        return DSA_ERR_UNSUPPORTED;
     *bytes = layout(op, batch, H, k).total;
     return DSA_OK;
 }
@@ -526,6 +553,133 @@ dsa_status_t dsa_decode_sink(const void *k_new, int k_dtype, const dsa_f16 *q_id
                              float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream) {
     return decode_impl(k_new, k_dtype, q_idx, w, q_lat, q_rope, k_cache, kv_cache, batch, H_I, H, k, sm_scale,
                        hadamard, n_sink, sink_pos0, out, lse, idx_out, ws, ws_bytes, stream);
+}
+
+
+// ---------------------------------------------------------------- kpool indexer
+
+static dsa_status_t check_kpool_cache(const dsa_batch_t *batch, const dsa_f16 *idx_rows, const dsa_f16 *pool_keys,
+                                      int64_t pool_rows) {
+    if (!idx_rows || !pool_keys) return DSA_ERR_INVALID_ARGUMENT;
+    if (pool_rows < 1 || pool_rows > INT32_MAX || pool_rows * kKpool < batch->max_kv) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(idx_rows, 2) || !aligned(pool_keys, 16)) return DSA_ERR_MISALIGNED;
+    return DSA_OK;
+}
+
+// The batch as the score and top-k kernels see it in pool mode.
+static DevBatch pool_batch(const dsa_batch_t *batch, int64_t pool_rows) {
+    DevBatch pb = dev_batch(batch);
+    pb.pool_log2 = kKpoolLog2;
+    pb.max_kv = std::max(1, batch->max_kv / kKpool);
+    pb.cache_rows = pool_rows;
+    return pb;
+}
+
+// Score windows of pools, their top-k, then the expansion into positions.
+static dsa_status_t kpool_select_impl(const dsa_f16 *q_idx, const float *w, const dsa_f16 *idx_rows,
+                                      const dsa_f16 *pool_keys, int64_t pool_rows, const dsa_batch_t *batch, int H_I,
+                                      int top_k, int32_t *idx, void *ws, const Layout &L, cudaStream_t stream,
+                                      bool after_append) {
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    uint32_t *st = status_ptr(ws);
+    const int kp = kpool_pools(top_k);
+    int32_t *pool_idx = reinterpret_cast<int32_t *>(w8 + L.pool_idx);
+    const DevBatch pb = pool_batch(batch, pool_rows);
+    bool pdl = after_append;
+    if (kp > 0) {
+        CUtensorMap km;
+        if (!make_map(&km, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pool_keys, D_I, (uint64_t)pool_rows, 64, 128))
+            return DSA_ERR_CUDA;
+        float *slab = reinterpret_cast<float *>(w8 + L.scores);
+        for (int j0 = 0; j0 < batch->max_q_per_seq; j0 += L.J) {
+            ScoreLaunch a{};
+            a.q_idx = q_idx;
+            a.w = w;
+            a.H_I = H_I;
+            a.scores = slab;
+            a.ld = L.ld;
+            a.rows = RowMap{1, j0, L.J};
+            // the append wrote only each token's own last pool: with one token
+            // per sequence the older pools' tiles need not wait for it
+            a.depends = after_append ? (j0 == 0 ? 1 : 2) : (j0 == 0 ? 0 : 2);
+            // one token per sequence: the top-k that follows is small
+            a.early_ok = batch->max_q_per_seq == 1 &&
+                         (int64_t)batch->batch * ((pb.max_kv + 8191) / 8192) <= kSMs / 4;
+            DSA_TRY_CUDA(launch_score(a, km, pb, st, stream, pdl || j0 > 0));
+            DSA_TRY_CUDA(launch_topk(slab, L.ld, pb, a.rows, kp, pool_idx, st, stream, true));
+            pdl = true;
+        }
+    }
+    DSA_TRY_CUDA(launch_kpool_expand(pool_idx, kp, idx_rows, dev_batch(batch), kpool_width(top_k), idx, st, stream,
+                                     pdl));
+    return DSA_OK;
+}
+
+dsa_status_t dsa_kpool_append(const dsa_f16 *k_new, const dsa_f16 *gate_new, const float *ape,
+                              const dsa_batch_t *batch, dsa_f16 *idx_rows, dsa_f16 *pool_keys, int64_t pool_rows,
+                              void *ws, size_t ws_bytes, cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!k_new || !gate_new || !ape) return DSA_ERR_INVALID_ARGUMENT;
+    if ((s = check_kpool_cache(batch, idx_rows, pool_keys, pool_rows)) != DSA_OK) return s;
+    if (!aligned(k_new, 16) || !aligned(gate_new, 16) || !aligned(ape, 4)) return DSA_ERR_MISALIGNED;
+    if ((s = check_ws(ws, ws_bytes, kStatusBytes)) != DSA_OK) return s;
+    const DevBatch db = dev_batch(batch);
+    const bool fused = batch->max_q_per_seq == 1;   // one token per sequence: rows and keys in one pass
+    DSA_TRY_CUDA(launch_kpool_append(k_new, gate_new, ape, db, idx_rows, pool_keys, pool_rows, 0, fused ? 1 : 0,
+                                     status_ptr(ws), stream));
+    if (!fused)
+        DSA_TRY_CUDA(launch_kpool_append(k_new, gate_new, ape, db, idx_rows, pool_keys, pool_rows, 1, 0,
+                                         status_ptr(ws), stream));
+    return DSA_OK;
+}
+
+dsa_status_t dsa_kpool_select(const dsa_f16 *q_idx, const float *w, const dsa_f16 *idx_rows,
+                              const dsa_f16 *pool_keys, int64_t pool_rows, const dsa_batch_t *batch, int H_I,
+                              int top_k, int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!q_idx || !w || !idx) return DSA_ERR_INVALID_ARGUMENT;
+    if (H_I < 1 || H_I > 64 || top_k < 1 || top_k > kKpoolMaxTopK) return DSA_ERR_UNSUPPORTED;
+    if ((s = check_kpool_cache(batch, idx_rows, pool_keys, pool_rows)) != DSA_OK) return s;
+    if (!aligned(q_idx, 16) || !aligned(w, 4) || !aligned(idx, 4)) return DSA_ERR_MISALIGNED;
+    const Layout L = layout(DSA_OP_KPOOL, batch, 64, top_k);
+    if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
+    return kpool_select_impl(q_idx, w, idx_rows, pool_keys, pool_rows, batch, H_I, top_k, idx, ws, L, stream, false);
+}
+
+dsa_status_t dsa_decode_kpool(const dsa_f16 *k_new, const dsa_f16 *gate_new, const float *ape,
+                              const dsa_f16 *q_idx, const float *w, const dsa_bf16 *q_lat, dsa_f16 *idx_rows,
+                              dsa_f16 *pool_keys, int64_t pool_rows, const dsa_bf16 *kv_latent,
+                              const dsa_batch_t *batch, int H_I, int H, int top_k, float sm_scale, float *out,
+                              float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    dsa_status_t s = check_batch(batch);
+    if (s != DSA_OK) return s;
+    if (!k_new || !gate_new || !ape || !q_idx || !w || !q_lat || !kv_latent || !out) return DSA_ERR_INVALID_ARGUMENT;
+    if (H_I < 1 || H_I > 64 || H < 1 || H > kMaxHeads || top_k < 1 || top_k > kKpoolMaxTopK)
+        return DSA_ERR_UNSUPPORTED;
+    if ((int64_t)batch->total_q * H > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    if ((s = check_kpool_cache(batch, idx_rows, pool_keys, pool_rows)) != DSA_OK) return s;
+    if (!aligned(k_new, 16) || !aligned(gate_new, 16) || !aligned(ape, 4) || !aligned(q_idx, 16) ||
+        !aligned(w, 4) || !aligned(q_lat, 16) || !aligned(kv_latent, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)) || (idx_out && !aligned(idx_out, 4)))
+        return DSA_ERR_MISALIGNED;
+    const Layout L = layout(DSA_OP_KPOOL, batch, H, top_k);
+    if ((s = check_ws(ws, ws_bytes, L.total)) != DSA_OK) return s;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(w8 + L.idx);
+    const DevBatch db = dev_batch(batch);
+    const bool fused = batch->max_q_per_seq == 1;
+    DSA_TRY_CUDA(launch_kpool_append(k_new, gate_new, ape, db, idx_rows, pool_keys, pool_rows, 0, fused ? 1 : 0,
+                                     status_ptr(ws), stream));
+    if (!fused)
+        DSA_TRY_CUDA(launch_kpool_append(k_new, gate_new, ape, db, idx_rows, pool_keys, pool_rows, 1, 0,
+                                         status_ptr(ws), stream));
+    if ((s = kpool_select_impl(q_idx, w, idx_rows, pool_keys, pool_rows, batch, H_I, top_k, idx, ws, L, stream,
+                               true)) != DSA_OK)
+        return s;
+    return run_attention(q_lat, nullptr, kv_latent, batch, idx, kpool_width(top_k), H, sm_scale, out, lse, ws, L,
+                         stream, false, true, nullptr, false);
 }
 
 }  // extern "C"

@@ -50,6 +50,11 @@ struct DevBatch {
     // kernels skip their copies so that the consumers' waits run out.
     uint64_t wait_ns;
     int skip_copies;
+    // Pool mode (kpool indexer): the score and top-k kernels work on pools
+    // of 2^pool_log2 positions -- a token at position p sees the complete
+    // pools 0 .. ((p + 1) >> pool_log2) - 1 (none: -1, an empty row, not an
+    // error) and sequence b's pools start at pool-cache row kv_off[b] >> pool_log2.
+    int pool_log2;
 };
 
 // Cache row of position pos (0 <= pos < max_kv) of sequence seq, whose
@@ -61,7 +66,18 @@ __device__ __forceinline__ int64_t cache_row(const DevBatch &b, int seq, int64_t
     return blk < 0 ? -1 : (int64_t)blk * b.block_size + pos % b.block_size;
 }
 __device__ __forceinline__ int64_t seq_base(const DevBatch &b, int seq) {
-    return b.kv_off ? __ldg(b.kv_off + seq) : 0;
+    const int64_t kv0 = b.kv_off ? __ldg(b.kv_off + seq) : 0;
+    return kv0 >> b.pool_log2;
+}
+// The last visible position (pool, in pool mode) of token t; -1 in pool mode
+// when no pool is complete yet.
+__device__ __forceinline__ int visible_last(const DevBatch &b, int t) {
+    const int p = __ldg(b.q_pos + t);
+    return b.pool_log2 ? ((p + 1) >> b.pool_log2) - 1 : p;
+}
+// A position that is out of range, as opposed to an empty row in pool mode.
+__device__ __forceinline__ bool bad_last(const DevBatch &b, int last) {
+    return b.pool_log2 ? last < -1 : last < 0;
 }
 
 // Tracing slots of the kernels (earliest CTA start, latest CTA end).
@@ -76,6 +92,21 @@ struct RowMap {
 
 cudaError_t launch_k_append(const void *k_new, int k_dtype, const DevBatch &b, uint16_t *k_cache,
                             int hadamard, uint32_t *status, cudaStream_t stream);
+
+// kpool indexer (GLM-5.3-Flash): packed rows k (128) | gate (128) | valid (1)
+// of kKpoolRow fp16 values, pools of kKpool positions.
+constexpr int kKpool = 4;
+constexpr int kKpoolLog2 = 2;
+constexpr int kKpoolRow = 257;
+// phase 0 writes the tokens' packed rows (and, when `fused`, the pooled key
+// of every pool a token completes); phase 1 writes only the pooled keys.
+cudaError_t launch_kpool_append(const uint16_t *k_new, const uint16_t *gate_new, const float *ape,
+                                const DevBatch &b, uint16_t *rows, uint16_t *pool_keys, int64_t pool_rows,
+                                int phase, int fused, uint32_t *status, cudaStream_t stream);
+// Selected pools (ascending, -1 padded, kp per token) -> token positions:
+// each pool's valid positions, then the valid tail positions, -1 padded to width.
+cudaError_t launch_kpool_expand(const int32_t *pool_idx, int kp, const uint16_t *rows, const DevBatch &b,
+                                int width, int32_t *idx, uint32_t *status, cudaStream_t stream, bool pdl);
 // In the launchers below `pdl` marks a launch that follows another kernel of
 // the same call (programmatic dependent launch).
 

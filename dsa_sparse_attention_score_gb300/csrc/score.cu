@@ -261,13 +261,14 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     if ((int)threadIdx.x < g) {                   // the group's positions, in parallel
         const int i = threadIdx.x;
         const int t = q0 + j_lo + i;
-        const int pos = __ldg(b.q_pos + t);
+        const int pos = visible_last(b, t);          // a pool index in pool mode
         bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0;
         if (ok) {
             const int64_t row = cache_row(b, seq, kv0, pos);
             ok = row >= 0 && row < b.cache_rows;
         }
-        if (!ok) flag(p.status, DSA_DEV_BAD_POSITION);
+        const bool empty = b.pool_log2 && pos == -1;  // no complete pool yet: nothing to score
+        if (!ok && !empty) flag(p.status, DSA_DEV_BAD_POSITION);
         sm.pos[i] = ok ? pos : -1;
         sm.out_row[i] = p.rows.slab ? (int64_t)seq * p.rows.J + (j_lo + i - p.rows.j0) : (int64_t)t;
     }
@@ -537,6 +538,10 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     tc_fence_before();
     __syncwarp();                  // lanes of warps 0 and 1 arrive from different paths
     __syncthreads();
+    // A CTA whose tiles did not depend on the preceding kernel never waited
+    // for it; waiting here keeps this grid from completing before it, so that
+    // kernels further down the stream may rely on it having completed too.
+    if (p.depends && threadIdx.x == 0) pdl_wait();
     if (!p.early) pdl_trigger();   // late: waiting dependents would share the SMs
     tl_end(b.timeline, kTlScore);
     if (warp == 1) {

@@ -330,7 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // streams are issued in whatever order their inputs arrive, so that an
         // O^T product (which frees a tile buffer for the next gather) never
         // waits behind a gather.
-        if (lane == 0 && wait_bar(smem_u32(&ctl.q_full), 0, ctl, p.status, b.wait_ns)) {
+        // Block (try_wait suspends the thread) until the queries and the first
+        // tile have landed: an early-launched grid would otherwise spin through
+        // the whole of the preceding kernels.
+        if (lane == 0 && wait_bar(smem_u32(&ctl.q_full), 0, ctl, p.status, b.wait_ns) &&
+            wait_bar(smem_u32(&ctl.c_full[0]), 0, ctl, p.status, b.wait_ns)) {
             const uint32_t id_s = idesc_f16(kRows, kHeads, true, false, false);
             const uint32_t id_o = idesc_f16(128, kHeads, true, true, true);
             const uint32_t qa = smem_u32(q_s), ca = smem_u32(c_s);
@@ -578,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
+    __syncwarp();                  // lanes of the MMA warp arrive from different paths
     __syncthreads();
     // Dependents launch only now: CTAs of the next grid waiting on this one
     // would share the SMs and slow it down.

@@ -262,10 +262,11 @@ __global__ void __launch_bounds__(NT) topk_cluster_kernel(const float *__restric
     const int t = row_token(b, rows, r);               // uniform over the cluster
     if (t >= 0) {
         int32_t *out = idx + (int64_t)t * k;
-        const int pos = __ldg(b.q_pos + t);
+        const int pos = visible_last(b, t);          // a pool index in pool mode
         const int g = (int)crank * NT + (int)threadIdx.x, GT = C * NT;
         if (pos < 0 || pos >= b.max_kv || (int64_t)pos >= ld) {
-            if (g == 0) flag(status, DSA_DEV_BAD_POSITION);
+            // (in pool mode -1 is a token with no complete pool: an empty row)
+            if (g == 0 && !(b.pool_log2 && pos == -1)) flag(status, DSA_DEV_BAD_POSITION);
             for (int i = g; i < k; i += GT) out[i] = -1;
         } else if (pos + 1 <= k) {
             for (int i = g; i < k; i += GT) out[i] = i <= pos ? i : -1;
@@ -294,9 +295,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
     const int t = row_token(b, rows, r);
     if (t >= 0) {
         int32_t *out = idx + (int64_t)t * k;
-        const int pos = __ldg(b.q_pos + t);
+        const int pos = visible_last(b, t);
         if (pos < 0 || pos >= b.max_kv || (int64_t)pos >= ld) {
-            if (tid == 0) flag(status, DSA_DEV_BAD_POSITION);
+            if (tid == 0 && !(b.pool_log2 && pos == -1)) flag(status, DSA_DEV_BAD_POSITION);
             for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
         } else if (pos + 1 <= k) {
             for (int i = tid; i < k; i += kTopkThreads) out[i] = i <= pos ? i : -1;

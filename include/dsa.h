@@ -92,7 +92,8 @@ enum {
     DSA_OP_INDEXER_SCORE = 1,
     DSA_OP_TOPK = 2,
     DSA_OP_SPARSE_ATTN = 3,
-    DSA_OP_DECODE = 4
+    DSA_OP_DECODE = 4,
+    DSA_OP_KPOOL = 5          /* dsa_kpool_select and dsa_decode_kpool (k = top_k) */
 };
 
 /*
@@ -314,6 +315,74 @@ dsa_status_t dsa_decode_noalloc(const void *k_new, int k_dtype, const dsa_f16 *q
                                 const dsa_batch_t *batch, int H_I, int H, int k, float sm_scale,
                                 int hadamard, float *out, float *lse, int32_t *idx_out,
                                 cudaStream_t stream);
+
+/*
+ * kpool indexer of GLM-5.3-Flash (vllm-rdna PR #2 "Glm5Next (GLM-5.3-Flash)
+ * on gfx1030", DSA layer bullet: kpool indexer 32h x 128, topk 2048, kpool 4,
+ * always_select_tail, pool compression softmax(gate+ape), tail <= 3 -> width
+ * 2051; two cache groups per DSA layer: the 512-wide latent and packed
+ * indexer rows of 257 = k|gate|valid).  Reading taken where the page is only
+ * an outline:
+ *  - pools are the aligned runs of 4 positions [4j, 4j+4) of a sequence; a
+ *    token at position p sees the complete pools j <= (p+1)/4 - 1; its tail
+ *    is the positions 4*floor((p+1)/4) .. p (at most 3);
+ *  - pooled key of pool j, per dim d: the softmax over the pool's valid rows
+ *    i of (gate[4j+i][d] + ape[i][d]) weighting k[4j+i][d], rounded once to
+ *    fp16 (computed in float64);
+ *  - pools are scored by the indexer formula on their pooled keys (no
+ *    rotation, no extra constant);
+ *  - top_k counts tokens: the floor(top_k/4) best pools by (score desc, pool
+ *    asc) are expanded to their valid positions and the valid tail positions
+ *    always added, ascending, -1 padded to width 4*floor(top_k/4) + 3 (2051
+ *    for top_k = 2048); the attention is the MLA-NoPE one over those rows.
+ * Caches:
+ *  idx_rows   fp16 [cache_rows, 257] (row stride 514 bytes): k (128) |
+ *             gate (128) | valid (1; 0.0 = absent row, anything else =
+ *             present); position s of sequence b at row kv_off[b] + s
+ *  pool_keys  fp16 [pool_rows, 128]: pool j of sequence b at row
+ *             kv_off[b]/4 + j; kv_off[b] must be a multiple of 4 and
+ *             pool_rows * 4 >= max_kv (else DSA_ERR_INVALID_ARGUMENT; a
+ *             kv_off that is not a multiple of 4 is flagged
+ *             DSA_DEV_BAD_POSITION and its tokens skipped)
+ *  ape        float32 [4, 128], the position-in-pool embedding
+ * Supported: 1 <= top_k <= 4096, 1 <= H_I <= 64, 1 <= H <= 128.
+ */
+
+/*
+ * Appends the tokens' packed rows (k_new | gate_new | 1.0 at kv_off[b] +
+ * q_pos[t]) and writes the pooled key of every pool a token completes
+ * (position = 3 mod 4), from the pool's rows as they are after the append.
+ *   k_new, gate_new  fp16 [T, 128] (16-byte aligned)
+ *   ws               at least dsa_workspace_size(DSA_OP_K_APPEND) bytes
+ */
+dsa_status_t dsa_kpool_append(const dsa_f16 *k_new, const dsa_f16 *gate_new, const float *ape,
+                              const dsa_batch_t *batch, dsa_f16 *idx_rows, dsa_f16 *pool_keys, int64_t pool_rows,
+                              void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The kpool selection of every token: scores of its complete pools (the
+ * indexer formula on pool_keys, q_idx [T,H_I,128] fp16, w [T,H_I] float32),
+ * the floor(top_k/4) best pools, expanded with the tail into positions:
+ *   idx   int32 [T, 4*floor(top_k/4) + 3], ascending, -1 padded
+ * Selected sets follow the tie rule of dsa_topk on float32 pool scores.
+ */
+dsa_status_t dsa_kpool_select(const dsa_f16 *q_idx, const float *w, const dsa_f16 *idx_rows,
+                              const dsa_f16 *pool_keys, int64_t pool_rows, const dsa_batch_t *batch, int H_I,
+                              int top_k, int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The fused GLM-5.3-Flash DSA step: dsa_kpool_append, dsa_kpool_select and
+ * MLA-NoPE attention (as dsa_sparse_mla_attn_nope) over the selected
+ * positions of kv_latent [cache_rows, 512] bf16, in that stream order.
+ *   q_lat [T,H,512] bf16, out [T,H,512] float32, lse [T,H] or NULL,
+ *   idx_out [T, 4*floor(top_k/4) + 3] int32 or NULL
+ * Workspace: dsa_workspace_size(DSA_OP_KPOOL, batch, H_I, H, top_k).
+ */
+dsa_status_t dsa_decode_kpool(const dsa_f16 *k_new, const dsa_f16 *gate_new, const float *ape,
+                              const dsa_f16 *q_idx, const float *w, const dsa_bf16 *q_lat, dsa_f16 *idx_rows,
+                              dsa_f16 *pool_keys, int64_t pool_rows, const dsa_bf16 *kv_latent,
+                              const dsa_batch_t *batch, int H_I, int H, int top_k, float sm_scale, float *out,
+                              float *lse, int32_t *idx_out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Workspace bytes an operation needs for this batch (host only; batch
