@@ -20,8 +20,12 @@
 // output order and copied out coalesced.  Output order is position order
 // because the cluster threads hold the row in order.
 //
-// Rows longer than 8 * 512 * 32 keys fall back to topk_kernel (one CTA per
-// row, keys staged in shared memory, see topk_impl.cuh).
+// Many rows longer than 16384 keys (k <= 4096), or any row longer than a
+// cluster holds, go to topk_stream_kernel: one CTA per row places a candidate
+// threshold from a sample of the row, streams the row once keeping the keys
+// at or above it, and selects exactly among those.  topk_kernel (one CTA per
+// row, keys staged in shared memory, see topk_impl.cuh) is the general
+// fallback.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 #include "topk_impl.cuh"
@@ -315,6 +319,225 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
 }
 
 namespace {
+constexpr int kStreamThreads = 512;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamSample = 4096;                        // sampled keys that place the threshold
+constexpr int kStreamWarpCap = 768;                        // candidates one warp may keep
+constexpr int kStreamCap = kStreamWarps * kStreamWarpCap;  // 12288
+constexpr size_t kStreamSmem = (size_t)kStreamCap * 8;     // candidate keys + positions: 96 KB
+constexpr int kStreamUnroll = 8;                           // 16-byte loads in flight per lane
+
+struct StreamSmem {
+    topk::Shared<kStreamThreads> sel;
+    uint32_t wcnt[kStreamWarps];                             // candidates kept per warp
+    uint32_t wgt[kStreamWarps], weq[kStreamWarps];           // per warp: keys above / equal to tau
+    uint32_t overflow;
+};
+}  // namespace
+
+// Exact top-k of long rows in one pass over the row (k <= kStreamCap / 3):
+//  A. the j-th largest of ~4096 evenly spaced sample keys, j about twice the
+//     expected sample rank of the row's k-th key, is a threshold tau_lo;
+//  B. every warp streams its contiguous segment of the row and appends the
+//     keys >= tau_lo, with their positions, in position order to its own
+//     region of shared memory;
+//  C. when at least k keys are kept, the row's k-th key is >= tau_lo, so every
+//     key the selection needs (and every key tied with the k-th) was kept: a
+//     three-digit radix select over the kept keys gives the exact tau;
+//  D. an ordered compaction of the kept keys writes the positions.
+// A region that overflows, or fewer than k kept keys, sends the row to the
+// general path (topk::select_row), so the result is exact whatever the data.
+__global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float *__restrict__ scores, int64_t ld,
+                                                                     DevBatch b, RowMap rows, int k,
+                                                                     int32_t *__restrict__ idx, uint32_t *status,
+                                                                     int n_sink, const int32_t *__restrict__ sink_pos0) {
+    __shared__ StreamSmem sm;
+    extern __shared__ uint32_t dyn[];                    // kept keys [kStreamCap], then their positions
+    uint32_t *ckey = dyn, *cpos = dyn + kStreamCap;
+    tl_start(b.timeline, kTlTopk);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t r = blockIdx.x;
+    const int t = row_token(b, rows, r);
+    if (t >= 0) {
+        int32_t *out = idx + (int64_t)t * k;
+        const int pos = visible_last(b, t);
+        if (pos < 0 || pos >= b.max_kv || (int64_t)pos >= ld) {
+            if (tid == 0 && !(b.pool_log2 && pos == -1)) flag(status, DSA_DEV_BAD_POSITION);
+            for (int i = tid; i < k; i += kStreamThreads) out[i] = -1;
+        } else if (pos + 1 <= k) {
+            for (int i = tid; i < k; i += kStreamThreads) out[i] = i <= pos ? i : -1;
+        } else {
+            int slo, shi;
+            row_sink(b, rows, r, t, n_sink, sink_pos0, slo, shi);
+            pdl_wait();                                  // the scores come from the preceding kernel
+            const int n = pos + 1;
+            const topk::RowSrc src{scores + r * ld, slo, shi};
+
+            // ---- A: sample threshold
+            const int m = min(n, kStreamSample);
+            {
+                uint32_t sk[kStreamSample / kStreamThreads];     // all of a thread's loads in flight at once
+#pragma unroll
+                for (int u = 0; u < kStreamSample / kStreamThreads; ++u) {
+                    const int i = tid + u * kStreamThreads;
+                    sk[u] = i < m ? topk::row_key(src, (int)((int64_t)i * n / m)) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < kStreamSample / kStreamThreads; ++u) {
+                    const int i = tid + u * kStreamThreads;
+                    if (i < m) ckey[i] = sk[u];
+                }
+            }
+            // about twice the sample rank of the row's k-th key, plus a margin
+            const int64_t jr = 2 * (((int64_t)k * m + n - 1) / n) + 16;
+            const int j = jr < m ? (int)jr : m;
+            uint32_t prefix = 0, kk = (uint32_t)j;
+            {
+                // digits of 11, 11 and 10 bits, from the top
+#pragma unroll 1
+                for (int pass = 0; pass < 3; ++pass) {
+                    const int sh = pass == 0 ? 21 : pass == 1 ? 10 : 0, wd = pass == 2 ? 10 : 11, nb = 1 << wd;
+                    topk::clear_hist(sm.sel, tid, nb);
+                    __syncthreads();
+                    topk::digit_hist<kStreamThreads, true>(sm.sel, tid, ckey, src, m, sh, nb, sh + wd, prefix);
+                    __syncthreads();
+                    topk::find_bin<kStreamThreads, -1>(sm.sel, tid, nb, kk);
+                    prefix = (prefix << wd) | sm.sel.sel_bin;
+                    kk -= sm.sel.sel_above;
+                    __syncthreads();
+                }
+            }
+            const uint32_t tau_lo = prefix;
+
+            // ---- B: one pass over the row, warp segments of whole 128-key steps
+            const int seg = ((n + kStreamWarps - 1) / kStreamWarps + 127) & ~127;
+            const int w0 = warp * seg, w1 = min(n, w0 + seg);
+            uint32_t *wk = ckey + warp * kStreamWarpCap, *wp = cpos + warp * kStreamWarpCap;
+            uint32_t wc = 0;
+            bool ovf = false;
+            const uint32_t lt = (1u << lane) - 1u;
+            for (int base = w0; base < w1; base += 128 * kStreamUnroll) {
+                float4 f[kStreamUnroll];
+#pragma unroll
+                for (int u = 0; u < kStreamUnroll; ++u) {
+                    // p0 < n <= ld and ld, p0 multiples of 4: the vector stays inside the row's stride
+                    const int p0 = base + u * 128 + 4 * lane;
+                    f[u] = p0 < w1 ? __ldcg(reinterpret_cast<const float4 *>(src.p + p0))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kStreamUnroll; ++u) {
+                    const int p0 = base + u * 128 + 4 * lane;
+                    const float fv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+                    uint32_t kv[4];
+                    uint32_t c = 0, mbits = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        kv[e] = src.sink(p0 + e) ? 0xFFFFFFFFu : float_key(fv[e]);
+                        const bool keep = p0 + e < w1 && kv[e] >= tau_lo;
+                        mbits |= (uint32_t)keep << e;
+                        c += keep;
+                    }
+                    uint32_t incl = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += v;
+                    }
+                    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+                    if (!ovf && wc + total <= (uint32_t)kStreamWarpCap) {
+                        uint32_t at = wc + incl - c;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if ((mbits >> e) & 1u) {
+                                wk[at] = kv[e];
+                                wp[at] = (uint32_t)(p0 + e);
+                                ++at;
+                            }
+                    } else {
+                        ovf = true;
+                    }
+                    wc += total;
+                }
+            }
+            if (lane == 0) sm.wcnt[warp] = ovf ? (uint32_t)kStreamWarpCap + 1u : wc;
+            __syncthreads();
+            uint32_t kept = 0;
+            bool bad = false;
+#pragma unroll
+            for (int w = 0; w < kStreamWarps; ++w) {
+                bad |= sm.wcnt[w] > (uint32_t)kStreamWarpCap;
+                kept += sm.wcnt[w];
+            }
+            bad |= kept < (uint32_t)k;                   // tau_lo above the k-th key: not enough kept
+
+            if (!bad) {
+                // ---- C: exact select among the kept keys
+                uint32_t tp = 0, above = 0;
+                kk = (uint32_t)k;
+#pragma unroll 1
+                for (int pass = 0; pass < 3; ++pass) {
+                    const int sh = pass == 0 ? 21 : pass == 1 ? 10 : 0, wd = pass == 2 ? 10 : 11;
+                    const int nb = 1 << wd, hsh = sh + wd;
+                    topk::clear_hist(sm.sel, tid, nb);
+                    __syncthreads();
+                    for (uint32_t i = lane; i < wc; i += 32) {       // each warp over its own kept keys
+                        const uint32_t key = wk[i];
+                        if (hsh >= 32 || (key >> hsh) == tp) atomicAdd(&sm.sel.hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+                    }
+                    __syncthreads();
+                    topk::find_bin<kStreamThreads, -1>(sm.sel, tid, nb, kk);
+                    tp = (tp << wd) | sm.sel.sel_bin;
+                    above += sm.sel.sel_above;
+                    kk -= sm.sel.sel_above;
+                    __syncthreads();
+                }
+                const uint32_t tau = tp, need_eq = (uint32_t)k - above;
+
+                // ---- D: ordered compaction, warp by warp over its region
+                uint32_t gt = 0, eq = 0;
+                for (uint32_t i0 = 0; i0 < wc; i0 += 32) {
+                    const uint32_t i = i0 + lane;
+                    const uint32_t key = i < wc ? wk[i] : 0u;
+                    gt += __popc(__ballot_sync(0xffffffffu, i < wc && key > tau));
+                    eq += __popc(__ballot_sync(0xffffffffu, i < wc && key == tau));
+                }
+                if (lane == 0) {
+                    sm.wgt[warp] = gt;
+                    sm.weq[warp] = eq;
+                }
+                __syncthreads();
+                uint32_t gt_before = 0, eq_before = 0;
+                for (int w = 0; w < warp; ++w) {
+                    gt_before += sm.wgt[w];
+                    eq_before += sm.weq[w];
+                }
+                uint32_t sel_before = gt_before + min(eq_before, need_eq);
+                for (uint32_t i0 = 0; i0 < wc; i0 += 32) {
+                    const uint32_t i = i0 + lane;
+                    const bool in = i < wc;
+                    const uint32_t key = in ? wk[i] : 0u;
+                    const bool is_gt = in && key > tau, is_eq = in && key == tau;
+                    const uint32_t eq_ballot = __ballot_sync(0xffffffffu, is_eq);
+                    const uint32_t eq_rank = eq_before + __popc(eq_ballot & lt);
+                    const bool sel = is_gt || (is_eq && eq_rank < need_eq);
+                    const uint32_t sel_ballot = __ballot_sync(0xffffffffu, sel);
+                    if (sel) out[sel_before + __popc(sel_ballot & lt)] = (int32_t)wp[i];
+                    eq_before += __popc(eq_ballot);
+                    sel_before += __popc(sel_ballot);
+                }
+            } else {
+                // the general path, with the whole dynamic shared memory as its key scratch
+                topk::select_row<kStreamThreads, -1>(sm.sel, tid, dyn, 2 * kStreamCap, src, n, k, out, nullptr);
+            }
+        }
+    }
+    __syncthreads();
+    pdl_trigger();
+    tl_end(b.timeline, kTlTopk);
+}
+
+namespace {
 
 template <int NT, int KPT>
 cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, RowMap rows, int k, int32_t *idx,
@@ -323,7 +546,7 @@ cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, R
     if (nrows * C > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const size_t stage = (size_t)std::min(k, NT * KPT) * 4;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_cluster_kernel<NT, KPT>),
-                                     NT == 256 ? 4 : (KPT == 16 ? 5 : 6), (size_t)NT * KPT * 4);
+                                     NT == 256 ? 5 : (KPT == 16 ? 6 : 7), (size_t)NT * KPT * 4);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nrows * C));
@@ -384,7 +607,18 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
             return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 256, 32, 1, n_sink, sink_pos0);
         return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 16, 1, n_sink, sink_pos0);
     }
-    if (n_max <= (int64_t)kMaxCluster * 512 * 32)
+    const bool vec = ld % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0;
+    const bool cluster_fits = n_max <= (int64_t)kMaxCluster * 512 * 32;
+    if (n_max > 512 * 32 && vec && k <= kStreamCap / 3 && (nrows >= kSMs || !cluster_fits)) {
+        // many long rows: one streaming pass per row (see topk_stream_kernel).
+        // Fewer rows than SMs keep the cluster path, which spreads a row's
+        // latency chain over several CTAs.
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_stream_kernel), 0, kStreamSmem);
+        if (e != cudaSuccess) return e;
+        return launch_k(topk_stream_kernel, dim3((unsigned)nrows), dim3(kStreamThreads), kStreamSmem, stream, pdl,
+                        scores, ld, b, rows, k, idx, status, n_sink, sink_pos0);
+    }
+    if (cluster_fits)
         return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 32,
                                (int)((n_max + 512 * 32 - 1) / (512 * 32)), n_sink, sink_pos0);
     int cap = kSmemCapHybrid;

@@ -135,9 +135,33 @@ def _topk_case(kind, rng):
         L = 70000 if kind == "cluster5" else 110000
         pos = [L - 1, L // 2, 16384, 16383, 5000]
         s = (rng.integers(-64, 64, (len(pos), L)) * 2.0 ** -6).astype(np.float32)   # many ties
-    elif kind == "beyond_cluster":              # longer than a cluster holds: shared-memory path
+    elif kind == "beyond_cluster":              # longer than a cluster holds: streaming path
         L, pos = 140000, [139999, 131072]
         s = rng.standard_normal((len(pos), L)).astype(np.float32)
+    elif kind == "beyond_cluster_unaligned":    # and not 16-byte aligned: shared-memory path
+        L, pos = 140001, [140000, 131072]
+        s = rng.standard_normal((len(pos), L)).astype(np.float32)
+    elif kind == "unaligned_cluster5":          # a row stride the 16-byte path cannot take: cluster of 5
+        L = 70001
+        pos = [L - 1, L // 2, 16384, 16383, 5000]
+        s = (rng.integers(-64, 64, (len(pos), L)) * 2.0 ** -6).astype(np.float32)
+    # at least as many long rows as SMs: the one-pass streaming path
+    elif kind == "stream_random":
+        L = 30000
+        pos = [L - 1 - 97 * i for i in range(152)] + [16384, 16383, 9000, 100]
+        s = rng.standard_normal((len(pos), L)).astype(np.float32)
+        s[:, 5000:5100] = 0.5                   # a run of ties
+    elif kind == "stream_all_equal":            # the pass keeps every key: the general path finishes
+        L = 40000
+        pos = [L - 1 - 13 * i for i in range(160)]
+        s = np.full((len(pos), L), 0.125, np.float32)
+    elif kind == "stream_sample_miss":          # the sampled keys are the largest: too few kept
+        L = 60000
+        pos = [L - 1 - 101 * i for i in range(160)]
+        s = rng.standard_normal((len(pos), L)).astype(np.float32)
+        for t, p in enumerate(pos):
+            n = p + 1
+            s[t, (np.arange(0, 4096, 20) * n) // 4096] = 100.0
     elif kind == "narrow":                      # distinct values that share high bits
         L, pos = 9000, [8999]
         s = (1.0 + rng.integers(0, 1 << 12, (1, L)) * 2.0 ** -23).astype(np.float32)
@@ -147,7 +171,9 @@ def _topk_case(kind, rng):
 
 
 @pytest.mark.parametrize("kind", ["random", "ties", "all_equal", "signed_zero", "neg_inf", "long_row", "narrow",
-                                  "cluster3", "cluster5", "cluster7", "beyond_cluster"])
+                                  "cluster3", "cluster5", "cluster7", "beyond_cluster", "beyond_cluster_unaligned",
+                                  "unaligned_cluster5",
+                                  "stream_random", "stream_all_equal", "stream_sample_miss"])
 @pytest.mark.parametrize("k", [1, 2048])
 def test_topk_bit_exact_on_oracle_scores(dsa, kind, k):
     import torch

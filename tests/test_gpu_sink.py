@@ -4,8 +4,8 @@ n_sink positions of each query's own sequence, counted from its first present
 position, always survive the top-k).
 
 dsa_topk_sink is checked bit-exact against the oracle on oracle-supplied
-scores, over the register (one CTA and cluster) and shared-memory paths;
-dsa_decode_sink end to end with the selection rule and attention tolerance of
+scores, over the register (one CTA and cluster), streaming and shared-memory
+paths; dsa_decode_sink end to end with the selection rule and attention tolerance of
 the other decode tests, plus the exact presence of every sink position.
 """
 import numpy as np
@@ -30,7 +30,9 @@ CASES = [
     # name, row length, positions, sequence boundaries (cu_q), anchors per sequence
     ("one_cta_unaligned", 5000, [4999, 3001, 2048, 2500], [0, 2, 4], [0, 37]),
     ("cluster3_aligned", 20000, [19999, 12000, 8192], [0, 3], [0]),
-    ("shared_memory_path", 140000, [139999, 131072], [0, 1, 2], [3, 0]),
+    ("beyond_cluster", 140000, [139999, 131072], [0, 1, 2], [3, 0]),
+    ("shared_memory_path", 140001, [140000, 131072], [0, 1, 2], [3, 0]),
+    ("streaming_path", 20000, [19999 - 61 * i for i in range(160)], [0, 80, 160], [0, 5]),
 ]
 
 
