@@ -321,39 +321,83 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
 namespace {
 constexpr int kStreamThreads = 512;
 constexpr int kStreamWarps = kStreamThreads / 32;
-constexpr int kStreamSample = 4096;                        // sampled keys that place the threshold
+constexpr int kStreamChunks = 128;                         // sampled runs of 32 keys: 4096 keys
+constexpr int kStreamSample = kStreamChunks * 32;
 constexpr int kStreamWarpCap = 768;                        // candidates one warp may keep
 constexpr int kStreamCap = kStreamWarps * kStreamWarpCap;  // 12288
-constexpr size_t kStreamSmem = (size_t)kStreamCap * 8;     // candidate keys + positions: 96 KB
+constexpr size_t kStreamSmem = (size_t)kStreamCap * 8;     // candidates (score bits, position): 96 KB
 constexpr int kStreamUnroll = 8;                           // 16-byte loads in flight per lane
 
 struct StreamSmem {
     topk::Shared<kStreamThreads> sel;
     uint32_t wcnt[kStreamWarps];                             // candidates kept per warp
     uint32_t wgt[kStreamWarps], weq[kStreamWarps];           // per warp: keys above / equal to tau
-    uint32_t overflow;
 };
+
+// The float whose key is `key` (the inverse of float_key).
+__device__ __forceinline__ float key_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Keeps the candidates of one 16-byte vector per lane (positions p0..p0+3),
+// appending them in position order to the warp's region.  A key is kept when
+// its score is not below tau_f (NaN scores are kept too: the exact passes
+// rank them by key).  kCheck: positions past w1 are dropped and attention-sink
+// positions always kept.
+template <bool kCheck>
+__device__ __forceinline__ void stream_keep(const float4 v, int p0, float tau_f, int w1, const topk::RowSrc &src,
+                                            uint32_t lt, uint2 *wc_buf, uint32_t &wc, bool &ovf) {
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    bool keep[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        keep[e] = !(f[e] < tau_f);
+        if (kCheck) keep[e] = p0 + e < w1 && (keep[e] || src.sink(p0 + e));
+    }
+    uint32_t bal[4], before = 0, total = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        bal[e] = __ballot_sync(0xffffffffu, keep[e]);
+        before += __popc(bal[e] & lt);
+        total += __popc(bal[e]);
+    }
+    if (total == 0) return;                              // warp-uniform
+    if (!ovf && wc + total <= (uint32_t)kStreamWarpCap) {
+        uint32_t at = wc + before;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (keep[e]) wc_buf[at++] = make_uint2(__float_as_uint(f[e]), (uint32_t)(p0 + e));
+    } else {
+        ovf = true;
+    }
+    wc += total;
+}
+
+// The key of a kept candidate: attention-sink positions rank first.
+__device__ __forceinline__ uint32_t cand_key(const uint2 c, const topk::RowSrc &src) {
+    return src.sink((int)c.y) ? 0xFFFFFFFFu : float_key(__uint_as_float(c.x));
+}
 }  // namespace
 
 // Exact top-k of long rows in one pass over the row (k <= kStreamCap / 3):
-//  A. the j-th largest of ~4096 evenly spaced sample keys, j about twice the
-//     expected sample rank of the row's k-th key, is a threshold tau_lo;
+//  A. the j-th largest of 4096 sample keys (128 evenly spaced runs of 32
+//     consecutive keys), j about twice the expected sample rank of the row's
+//     k-th key, is a threshold tau_lo;
 //  B. every warp streams its contiguous segment of the row and appends the
-//     keys >= tau_lo, with their positions, in position order to its own
-//     region of shared memory;
+//     scores not below tau_lo, with their positions, in position order to
+//     its own region of shared memory;
 //  C. when at least k keys are kept, the row's k-th key is >= tau_lo, so every
 //     key the selection needs (and every key tied with the k-th) was kept: a
 //     three-digit radix select over the kept keys gives the exact tau;
 //  D. an ordered compaction of the kept keys writes the positions.
 // A region that overflows, or fewer than k kept keys, sends the row to the
 // general path (topk::select_row), so the result is exact whatever the data.
-__global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float *__restrict__ scores, int64_t ld,
-                                                                     DevBatch b, RowMap rows, int k,
-                                                                     int32_t *__restrict__ idx, uint32_t *status,
-                                                                     int n_sink, const int32_t *__restrict__ sink_pos0) {
+__global__ void __launch_bounds__(kStreamThreads, 2)
+    topk_stream_kernel(const float *__restrict__ scores, int64_t ld, DevBatch b, RowMap rows, int k,
+                       int32_t *__restrict__ idx, uint32_t *status, int n_sink, const int32_t *__restrict__ sink_pos0) {
     __shared__ StreamSmem sm;
-    extern __shared__ uint32_t dyn[];                    // kept keys [kStreamCap], then their positions
-    uint32_t *ckey = dyn, *cpos = dyn + kStreamCap;
+    extern __shared__ uint2 cand[];                      // kept (score bits, position) [kStreamCap]
+    uint32_t *skey = reinterpret_cast<uint32_t *>(cand);  // the samples' keys, before the pass
     tl_start(b.timeline, kTlTopk);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t r = blockIdx.x;
@@ -376,16 +420,20 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float
             // ---- A: sample threshold
             const int m = min(n, kStreamSample);
             {
-                uint32_t sk[kStreamSample / kStreamThreads];     // all of a thread's loads in flight at once
+                // every key of a short row, else run c of 32 keys from (c (n - 32) / 127) rounded down to 32
+                uint32_t sk[kStreamSample / kStreamThreads];
 #pragma unroll
                 for (int u = 0; u < kStreamSample / kStreamThreads; ++u) {
                     const int i = tid + u * kStreamThreads;
-                    sk[u] = i < m ? topk::row_key(src, (int)((int64_t)i * n / m)) : 0u;
+                    const int s = n <= kStreamSample
+                                      ? i
+                                      : ((int)((int64_t)(i >> 5) * (n - 32) / (kStreamChunks - 1)) & ~31) + (i & 31);
+                    sk[u] = i < m ? topk::row_key(src, s) : 0u;
                 }
 #pragma unroll
                 for (int u = 0; u < kStreamSample / kStreamThreads; ++u) {
                     const int i = tid + u * kStreamThreads;
-                    if (i < m) ckey[i] = sk[u];
+                    if (i < m) skey[i] = sk[u];
                 }
             }
             // about twice the sample rank of the row's k-th key, plus a margin
@@ -399,7 +447,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float
                     const int sh = pass == 0 ? 21 : pass == 1 ? 10 : 0, wd = pass == 2 ? 10 : 11, nb = 1 << wd;
                     topk::clear_hist(sm.sel, tid, nb);
                     __syncthreads();
-                    topk::digit_hist<kStreamThreads, true>(sm.sel, tid, ckey, src, m, sh, nb, sh + wd, prefix);
+                    topk::digit_hist<kStreamThreads, true>(sm.sel, tid, skey, src, m, sh, nb, sh + wd, prefix);
                     __syncthreads();
                     topk::find_bin<kStreamThreads, -1>(sm.sel, tid, nb, kk);
                     prefix = (prefix << wd) | sm.sel.sel_bin;
@@ -407,58 +455,39 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float
                     __syncthreads();
                 }
             }
-            const uint32_t tau_lo = prefix;
+            const float tau_f = key_float(prefix);       // keys >= prefix <=> scores not below tau_f
 
             // ---- B: one pass over the row, warp segments of whole 128-key steps
             const int seg = ((n + kStreamWarps - 1) / kStreamWarps + 127) & ~127;
-            const int w0 = warp * seg, w1 = min(n, w0 + seg);
-            uint32_t *wk = ckey + warp * kStreamWarpCap, *wp = cpos + warp * kStreamWarpCap;
+            const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
+            uint2 *wbuf = cand + warp * kStreamWarpCap;
             uint32_t wc = 0;
             bool ovf = false;
             const uint32_t lt = (1u << lane) - 1u;
-            for (int base = w0; base < w1; base += 128 * kStreamUnroll) {
-                float4 f[kStreamUnroll];
+            const float4 *vp = reinterpret_cast<const float4 *>(src.p);   // ld % 4 == 0: rows stay 16-byte aligned
+            int base = w0;
+            if (!(src.lo < src.hi && src.lo < w1 && src.hi > w0)) {
+                // whole blocks with no sink position: no per-key checks
+                for (; base + 128 * kStreamUnroll <= w1; base += 128 * kStreamUnroll) {
+                    float4 v[kStreamUnroll];
+#pragma unroll
+                    for (int u = 0; u < kStreamUnroll; ++u) v[u] = __ldcg(vp + ((base >> 2) + u * 32 + lane));
+#pragma unroll
+                    for (int u = 0; u < kStreamUnroll; ++u)
+                        stream_keep<false>(v[u], base + u * 128 + 4 * lane, tau_f, w1, src, lt, wbuf, wc, ovf);
+                }
+            }
+            for (; base < w1; base += 128 * kStreamUnroll) {
+                float4 v[kStreamUnroll];
 #pragma unroll
                 for (int u = 0; u < kStreamUnroll; ++u) {
-                    // p0 < n <= ld and ld, p0 multiples of 4: the vector stays inside the row's stride
+                    // p0 (a multiple of 4) < w1 <= ld (a multiple of 4): the vector stays inside the row's stride
                     const int p0 = base + u * 128 + 4 * lane;
-                    f[u] = p0 < w1 ? __ldcg(reinterpret_cast<const float4 *>(src.p + p0))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[u] = p0 < w1 ? __ldcg(vp + (p0 >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
-                for (int u = 0; u < kStreamUnroll; ++u) {
-                    const int p0 = base + u * 128 + 4 * lane;
-                    const float fv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
-                    uint32_t kv[4];
-                    uint32_t c = 0, mbits = 0;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        kv[e] = src.sink(p0 + e) ? 0xFFFFFFFFu : float_key(fv[e]);
-                        const bool keep = p0 + e < w1 && kv[e] >= tau_lo;
-                        mbits |= (uint32_t)keep << e;
-                        c += keep;
-                    }
-                    uint32_t incl = c;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += v;
-                    }
-                    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-                    if (!ovf && wc + total <= (uint32_t)kStreamWarpCap) {
-                        uint32_t at = wc + incl - c;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if ((mbits >> e) & 1u) {
-                                wk[at] = kv[e];
-                                wp[at] = (uint32_t)(p0 + e);
-                                ++at;
-                            }
-                    } else {
-                        ovf = true;
-                    }
-                    wc += total;
-                }
+                for (int u = 0; u < kStreamUnroll; ++u)
+                    stream_keep<true>(v[u], base + u * 128 + 4 * lane, tau_f, w1, src, lt, wbuf, wc, ovf);
             }
             if (lane == 0) sm.wcnt[warp] = ovf ? (uint32_t)kStreamWarpCap + 1u : wc;
             __syncthreads();
@@ -482,7 +511,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float
                     topk::clear_hist(sm.sel, tid, nb);
                     __syncthreads();
                     for (uint32_t i = lane; i < wc; i += 32) {       // each warp over its own kept keys
-                        const uint32_t key = wk[i];
+                        const uint32_t key = cand_key(wbuf[i], src);
                         if (hsh >= 32 || (key >> hsh) == tp) atomicAdd(&sm.sel.hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
                     }
                     __syncthreads();
@@ -498,7 +527,7 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float
                 uint32_t gt = 0, eq = 0;
                 for (uint32_t i0 = 0; i0 < wc; i0 += 32) {
                     const uint32_t i = i0 + lane;
-                    const uint32_t key = i < wc ? wk[i] : 0u;
+                    const uint32_t key = i < wc ? cand_key(wbuf[i], src) : 0u;
                     gt += __popc(__ballot_sync(0xffffffffu, i < wc && key > tau));
                     eq += __popc(__ballot_sync(0xffffffffu, i < wc && key == tau));
                 }
@@ -516,19 +545,21 @@ __global__ void __launch_bounds__(kStreamThreads) topk_stream_kernel(const float
                 for (uint32_t i0 = 0; i0 < wc; i0 += 32) {
                     const uint32_t i = i0 + lane;
                     const bool in = i < wc;
-                    const uint32_t key = in ? wk[i] : 0u;
+                    const uint2 c = in ? wbuf[i] : make_uint2(0u, 0u);
+                    const uint32_t key = in ? cand_key(c, src) : 0u;
                     const bool is_gt = in && key > tau, is_eq = in && key == tau;
                     const uint32_t eq_ballot = __ballot_sync(0xffffffffu, is_eq);
                     const uint32_t eq_rank = eq_before + __popc(eq_ballot & lt);
                     const bool sel = is_gt || (is_eq && eq_rank < need_eq);
                     const uint32_t sel_ballot = __ballot_sync(0xffffffffu, sel);
-                    if (sel) out[sel_before + __popc(sel_ballot & lt)] = (int32_t)wp[i];
+                    if (sel) out[sel_before + __popc(sel_ballot & lt)] = (int32_t)c.y;
                     eq_before += __popc(eq_ballot);
                     sel_before += __popc(sel_ballot);
                 }
             } else {
                 // the general path, with the whole dynamic shared memory as its key scratch
-                topk::select_row<kStreamThreads, -1>(sm.sel, tid, dyn, 2 * kStreamCap, src, n, k, out, nullptr);
+                topk::select_row<kStreamThreads, -1>(sm.sel, tid, reinterpret_cast<uint32_t *>(cand), 2 * kStreamCap,
+                                                     src, n, k, out, nullptr);
             }
         }
     }
