@@ -319,19 +319,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *__restr
 }
 
 namespace {
-constexpr int kStreamThreads = 512;
-constexpr int kStreamWarps = kStreamThreads / 32;
-constexpr int kStreamChunks = 128;                         // sampled runs of 32 keys: 4096 keys
-constexpr int kStreamSample = kStreamChunks * 32;
-constexpr int kStreamWarpCap = 768;                        // candidates one warp may keep
-constexpr int kStreamCap = kStreamWarps * kStreamWarpCap;  // 12288
-constexpr size_t kStreamSmem = (size_t)kStreamCap * 8;     // candidates (score bits, position): 96 KB
-constexpr int kStreamUnroll = 8;                           // 16-byte loads in flight per lane
+constexpr int kStreamRun = 16;                             // sampled runs of 16 keys (one 64-byte line) ...
+constexpr int kStreamRuns = 256;                           // ... 4096 keys
+constexpr int kStreamSample = kStreamRuns * kStreamRun;
+// Shared memory of the candidates (score bits, position) of NT threads
+// whose warps keep at most WCAP each.
+template <int NT, int WCAP>
+constexpr size_t stream_smem() { return (size_t)(NT / 32) * WCAP * 8; }
+constexpr int kStreamUnroll = 5;                           // 128-key groups in flight per warp
 
+template <int NT>
 struct StreamSmem {
-    topk::Shared<kStreamThreads> sel;
-    uint32_t wcnt[kStreamWarps];                             // candidates kept per warp
-    uint32_t wgt[kStreamWarps], weq[kStreamWarps];           // per warp: keys above / equal to tau
+    topk::Shared<NT> sel;
+    uint32_t wcnt[NT / 32];                                  // candidates kept per warp
+    uint32_t wgt[NT / 32], weq[NT / 32];                     // per warp: keys above / equal to tau
 };
 
 // The float whose key is `key` (the inverse of float_key).
@@ -339,38 +340,21 @@ __device__ __forceinline__ float key_float(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// Keeps the candidates of one 16-byte vector per lane (positions p0..p0+3),
-// appending them in position order to the warp's region.  A key is kept when
-// its score is not below tau_f (NaN scores are kept too: the exact passes
-// rank them by key).  kCheck: positions past w1 are dropped and attention-sink
-// positions always kept.
-template <bool kCheck>
-__device__ __forceinline__ void stream_keep(const float4 v, int p0, float tau_f, int w1, const topk::RowSrc &src,
-                                            uint32_t lt, uint2 *wc_buf, uint32_t &wc, bool &ovf) {
-    const float f[4] = {v.x, v.y, v.z, v.w};
-    bool keep[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        keep[e] = !(f[e] < tau_f);
-        if (kCheck) keep[e] = p0 + e < w1 && (keep[e] || src.sink(p0 + e));
-    }
-    uint32_t bal[4], before = 0, total = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        bal[e] = __ballot_sync(0xffffffffu, keep[e]);
-        before += __popc(bal[e] & lt);
-        total += __popc(bal[e]);
-    }
-    if (total == 0) return;                              // warp-uniform
-    if (!ovf && wc + total <= (uint32_t)kStreamWarpCap) {
-        uint32_t at = wc + before;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (keep[e]) wc_buf[at++] = make_uint2(__float_as_uint(f[e]), (uint32_t)(p0 + e));
-    } else {
-        ovf = true;
-    }
-    wc += total;
+// Keeps the candidate at position p of one 32-key step of a warp (lane i
+// holds position step + i), appending it to the warp's region in position
+// order.  A key is kept when its score is not below tau_f (NaN scores are
+// kept too: the exact passes rank them by key).  Appends past the region's
+// capacity are dropped; the count wc still grows, which marks the overflow.
+// kCheck: positions past w1 are dropped and attention-sink positions kept.
+template <int WCAP, bool kCheck>
+__device__ __forceinline__ void stream_keep(float f, int p, float tau_f, int w1, const topk::RowSrc &src,
+                                            uint32_t lt, uint2 *wbuf, uint32_t &wc) {
+    bool keep = !(f < tau_f);
+    if (kCheck) keep = p < w1 && (keep || src.sink(p));
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+    const uint32_t at = wc + __popc(bal & lt);
+    if (keep && at < (uint32_t)WCAP) wbuf[at] = make_uint2(__float_as_uint(f), (uint32_t)p);
+    wc += __popc(bal);
 }
 
 // The key of a kept candidate: attention-sink positions rank first.
@@ -379,10 +363,11 @@ __device__ __forceinline__ uint32_t cand_key(const uint2 c, const topk::RowSrc &
 }
 }  // namespace
 
-// Exact top-k of long rows in one pass over the row (k <= kStreamCap / 3):
-//  A. the j-th largest of 4096 sample keys (128 evenly spaced runs of 32
-//     consecutive keys), j about twice the expected sample rank of the row's
-//     k-th key, is a threshold tau_lo;
+// Exact top-k of long rows in one pass over the row, by one CTA of NT threads
+// whose warps keep at most WCAP candidates each:
+//  A. a lower bound (22 leading bits) of the j-th largest of 4096 sample keys
+//     (256 evenly spaced runs of 16 consecutive keys), j about 1.5 times
+//     the expected sample rank of the row's k-th key, is a threshold tau_lo;
 //  B. every warp streams its contiguous segment of the row and appends the
 //     scores not below tau_lo, with their positions, in position order to
 //     its own region of shared memory;
@@ -392,11 +377,13 @@ __device__ __forceinline__ uint32_t cand_key(const uint2 c, const topk::RowSrc &
 //  D. an ordered compaction of the kept keys writes the positions.
 // A region that overflows, or fewer than k kept keys, sends the row to the
 // general path (topk::select_row), so the result is exact whatever the data.
-__global__ void __launch_bounds__(kStreamThreads, 2)
+template <int NT, int WCAP>
+__global__ void __launch_bounds__(NT, 1024 / NT)
     topk_stream_kernel(const float *__restrict__ scores, int64_t ld, DevBatch b, RowMap rows, int k,
                        int32_t *__restrict__ idx, uint32_t *status, int n_sink, const int32_t *__restrict__ sink_pos0) {
-    __shared__ StreamSmem sm;
-    extern __shared__ uint2 cand[];                      // kept (score bits, position) [kStreamCap]
+    constexpr int W = NT / 32;
+    __shared__ StreamSmem<NT> sm;
+    extern __shared__ uint2 cand[];                      // kept (score bits, position) [W * WCAP]
     uint32_t *skey = reinterpret_cast<uint32_t *>(cand);  // the samples' keys, before the pass
     tl_start(b.timeline, kTlTopk);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -407,9 +394,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         const int pos = visible_last(b, t);
         if (pos < 0 || pos >= b.max_kv || (int64_t)pos >= ld) {
             if (tid == 0 && !(b.pool_log2 && pos == -1)) flag(status, DSA_DEV_BAD_POSITION);
-            for (int i = tid; i < k; i += kStreamThreads) out[i] = -1;
+            for (int i = tid; i < k; i += NT) out[i] = -1;
         } else if (pos + 1 <= k) {
-            for (int i = tid; i < k; i += kStreamThreads) out[i] = i <= pos ? i : -1;
+            for (int i = tid; i < k; i += NT) out[i] = i <= pos ? i : -1;
         } else {
             int slo, shi;
             row_sink(b, rows, r, t, n_sink, sink_pos0, slo, shi);
@@ -420,82 +407,86 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             // ---- A: sample threshold
             const int m = min(n, kStreamSample);
             {
-                // every key of a short row, else run c of 32 keys from (c (n - 32) / 127) rounded down to 32
-                uint32_t sk[kStreamSample / kStreamThreads];
+                // every key of a short row, else run c of 16 keys from c (n - 16) / 255 rounded down to 16
+                uint32_t sk[kStreamSample / NT];
+                const uint32_t run_step = (uint32_t)(n - kStreamRun) / (kStreamRuns - 1);
+                const uint32_t run_rem = (uint32_t)(n - kStreamRun) % (kStreamRuns - 1);
 #pragma unroll
-                for (int u = 0; u < kStreamSample / kStreamThreads; ++u) {
-                    const int i = tid + u * kStreamThreads;
+                for (int u = 0; u < kStreamSample / NT; ++u) {
+                    const int i = tid + u * NT;
+                    const uint32_t c = (uint32_t)i / kStreamRun;
+                    // c (n - 16) / 255 without 64-bit arithmetic: c step + c rem / 255
                     const int s = n <= kStreamSample
                                       ? i
-                                      : ((int)((int64_t)(i >> 5) * (n - 32) / (kStreamChunks - 1)) & ~31) + (i & 31);
+                                      : (int)((c * run_step + c * run_rem / (kStreamRuns - 1)) & ~(uint32_t)(kStreamRun - 1)) +
+                                            (i & (kStreamRun - 1));
                     sk[u] = i < m ? topk::row_key(src, s) : 0u;
                 }
 #pragma unroll
-                for (int u = 0; u < kStreamSample / kStreamThreads; ++u) {
-                    const int i = tid + u * kStreamThreads;
+                for (int u = 0; u < kStreamSample / NT; ++u) {
+                    const int i = tid + u * NT;
                     if (i < m) skey[i] = sk[u];
                 }
             }
-            // about twice the sample rank of the row's k-th key, plus a margin
-            const int64_t jr = 2 * (((int64_t)k * m + n - 1) / n) + 16;
+            // about 1.5 times the sample rank of the row's k-th key, plus a margin
+            const int64_t jr = 3 * (((int64_t)k * m + n - 1) / n) / 2 + 16;
             const int j = jr < m ? (int)jr : m;
             uint32_t prefix = 0, kk = (uint32_t)j;
             {
-                // digits of 11, 11 and 10 bits, from the top
+                // two digits of 11 bits, from the top: the bin holding the j-th largest sample
 #pragma unroll 1
-                for (int pass = 0; pass < 3; ++pass) {
-                    const int sh = pass == 0 ? 21 : pass == 1 ? 10 : 0, wd = pass == 2 ? 10 : 11, nb = 1 << wd;
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int sh = pass == 0 ? 21 : 10, wd = 11, nb = 1 << wd;
                     topk::clear_hist(sm.sel, tid, nb);
                     __syncthreads();
-                    topk::digit_hist<kStreamThreads, true>(sm.sel, tid, skey, src, m, sh, nb, sh + wd, prefix);
+                    topk::digit_hist<NT, true>(sm.sel, tid, skey, src, m, sh, nb, sh + wd, prefix);
                     __syncthreads();
-                    topk::find_bin<kStreamThreads, -1>(sm.sel, tid, nb, kk);
+                    topk::find_bin<NT, -1>(sm.sel, tid, nb, kk);
                     prefix = (prefix << wd) | sm.sel.sel_bin;
                     kk -= sm.sel.sel_above;
                     __syncthreads();
                 }
             }
+            prefix <<= 10;                               // the bin's lowest key
             const float tau_f = key_float(prefix);       // keys >= prefix <=> scores not below tau_f
 
-            // ---- B: one pass over the row, warp segments of whole 128-key steps
-            const int seg = ((n + kStreamWarps - 1) / kStreamWarps + 127) & ~127;
+            // ---- B: one pass over the row, warp segments of whole 128-key groups
+            const int seg = ((n + W - 1) / W + 127) & ~127;
             const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
-            uint2 *wbuf = cand + warp * kStreamWarpCap;
+            uint2 *wbuf = cand + warp * WCAP;
             uint32_t wc = 0;
-            bool ovf = false;
             const uint32_t lt = (1u << lane) - 1u;
-            const float4 *vp = reinterpret_cast<const float4 *>(src.p);   // ld % 4 == 0: rows stay 16-byte aligned
             int base = w0;
             if (!(src.lo < src.hi && src.lo < w1 && src.hi > w0)) {
                 // whole blocks with no sink position: no per-key checks
                 for (; base + 128 * kStreamUnroll <= w1; base += 128 * kStreamUnroll) {
-                    float4 v[kStreamUnroll];
+                    float v[4 * kStreamUnroll];
 #pragma unroll
-                    for (int u = 0; u < kStreamUnroll; ++u) v[u] = __ldcg(vp + ((base >> 2) + u * 32 + lane));
+                    for (int u = 0; u < 4 * kStreamUnroll; ++u) v[u] = __ldcg(src.p + base + 32 * u + lane);
 #pragma unroll
-                    for (int u = 0; u < kStreamUnroll; ++u)
-                        stream_keep<false>(v[u], base + u * 128 + 4 * lane, tau_f, w1, src, lt, wbuf, wc, ovf);
+                    for (int u = 0; u < 4 * kStreamUnroll; ++u)
+                        stream_keep<WCAP, false>(v[u], base + 32 * u + lane, tau_f, w1, src, lt, wbuf, wc);
                 }
             }
             for (; base < w1; base += 128 * kStreamUnroll) {
-                float4 v[kStreamUnroll];
+                float v[4 * kStreamUnroll];
 #pragma unroll
-                for (int u = 0; u < kStreamUnroll; ++u) {
-                    // p0 (a multiple of 4) < w1 <= ld (a multiple of 4): the vector stays inside the row's stride
-                    const int p0 = base + u * 128 + 4 * lane;
-                    v[u] = p0 < w1 ? __ldcg(vp + (p0 >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int u = 0; u < 4 * kStreamUnroll; ++u) {
+                    const int p = base + 32 * u + lane;
+                    v[u] = p < w1 ? __ldcg(src.p + p) : 0.f;
                 }
 #pragma unroll
-                for (int u = 0; u < kStreamUnroll; ++u)
-                    stream_keep<true>(v[u], base + u * 128 + 4 * lane, tau_f, w1, src, lt, wbuf, wc, ovf);
+                for (int u = 0; u < 4 * kStreamUnroll; ++u)
+                    stream_keep<WCAP, true>(v[u], base + 32 * u + lane, tau_f, w1, src, lt, wbuf, wc);
             }
-            if (lane == 0) sm.wcnt[warp] = ovf ? (uint32_t)kStreamWarpCap + 1u : wc;
+            const bool ovf = wc > (uint32_t)WCAP;
+            if (lane == 0) sm.wcnt[warp] = ovf ? (uint32_t)WCAP + 1u : wc;
             __syncthreads();
             uint32_t kept = 0;
             bool bad = false;
 #pragma unroll
-            for (int w = 0; w < kStreamWarps; ++w) {
-                bad |= sm.wcnt[w] > (uint32_t)kStreamWarpCap;
+            for (int w = 0; w < W; ++w) {
+                bad |= sm.wcnt[w] > (uint32_t)WCAP;
                 kept += sm.wcnt[w];
             }
             bad |= kept < (uint32_t)k;                   // tau_lo above the k-th key: not enough kept
@@ -515,7 +506,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                         if (hsh >= 32 || (key >> hsh) == tp) atomicAdd(&sm.sel.hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
                     }
                     __syncthreads();
-                    topk::find_bin<kStreamThreads, -1>(sm.sel, tid, nb, kk);
+                    topk::find_bin<NT, -1>(sm.sel, tid, nb, kk);
                     tp = (tp << wd) | sm.sel.sel_bin;
                     above += sm.sel.sel_above;
                     kk -= sm.sel.sel_above;
@@ -558,7 +549,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 }
             } else {
                 // the general path, with the whole dynamic shared memory as its key scratch
-                topk::select_row<kStreamThreads, -1>(sm.sel, tid, reinterpret_cast<uint32_t *>(cand), 2 * kStreamCap,
+                topk::select_row<NT, -1>(sm.sel, tid, reinterpret_cast<uint32_t *>(cand), 2 * W * WCAP,
                                                      src, n, k, out, nullptr);
             }
         }
@@ -566,6 +557,17 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     __syncthreads();
     pdl_trigger();
     tl_end(b.timeline, kTlTopk);
+}
+
+template <int NT, int WCAP>
+cudaError_t launch_stream(const float *scores, int64_t ld, const DevBatch &b, const RowMap &rows, int k, int32_t *idx,
+                          uint32_t *status, cudaStream_t stream, bool pdl, int64_t nrows, int n_sink,
+                          const int32_t *sink_pos0, int slot) {
+    constexpr size_t smem = stream_smem<NT, WCAP>();
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_stream_kernel<NT, WCAP>), slot, smem);
+    if (e != cudaSuccess) return e;
+    return launch_k(topk_stream_kernel<NT, WCAP>, dim3((unsigned)nrows), dim3(NT), smem, stream, pdl, scores, ld, b,
+                    rows, k, idx, status, n_sink, sink_pos0);
 }
 
 namespace {
@@ -640,14 +642,15 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
     }
     const bool vec = ld % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0;
     const bool cluster_fits = n_max <= (int64_t)kMaxCluster * 512 * 32;
-    if (n_max > 512 * 32 && vec && k <= kStreamCap / 3 && (nrows >= kSMs || !cluster_fits)) {
+    if (n_max > 512 * 32 && vec && k <= 4096 && (nrows >= kSMs || !cluster_fits)) {
         // many long rows: one streaming pass per row (see topk_stream_kernel).
         // Fewer rows than SMs keep the cluster path, which spreads a row's
-        // latency chain over several CTAs.
-        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_stream_kernel), 0, kStreamSmem);
-        if (e != cudaSuccess) return e;
-        return launch_k(topk_stream_kernel, dim3((unsigned)nrows), dim3(kStreamThreads), kStreamSmem, stream, pdl,
-                        scores, ld, b, rows, k, idx, status, n_sink, sink_pos0);
+        // latency chain over several CTAs.  Four CTAs of 256 threads share an
+        // SM when k <= 2048 (so that one row's selection overlaps the others'
+        // passes), two of 512 up to k = 4096.
+        if (k <= 2048) return launch_stream<256, 704>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, n_sink,
+                                                      sink_pos0, 8);
+        return launch_stream<512, 768>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, n_sink, sink_pos0, 0);
     }
     if (cluster_fits)
         return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 32,

@@ -192,6 +192,13 @@ def test_topk_bit_exact_on_oracle_scores(dsa, kind, k):
     _status_clean(dsa, ws)
 
 
+@pytest.mark.parametrize("kind", ["stream_random", "stream_sample_miss"])
+@pytest.mark.parametrize("k", [2049, 4096])
+def test_topk_streaming_large_k(dsa, kind, k):
+    """k above 2048 takes the streaming kernel's 512-thread configuration."""
+    test_topk_bit_exact_on_oracle_scores(dsa, kind, k)
+
+
 def test_topk_short_rows_and_k_boundaries(dsa):
     import torch
     rng = np.random.default_rng(5)
