@@ -74,6 +74,9 @@ def parse():
     ap.add_argument("--headline-only", action="store_true",
                     help="measure only the chosen workload (by default the batched-decode run also measures the "
                          "ragged decode and the two prefill workloads)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="prefill workloads only: keep the last N query tokens of the chunk (same row lengths, "
+                         "a smaller case of the same kernels, e.g. for an ncu capture)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each step as a CUDA graph (default: the library's own stream launches, which "
                          "measured 2.8 us faster per batched-decode step on GB300: a graph replay adds "
@@ -91,6 +94,19 @@ def peaks():
                     bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
                     source="measured")
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def shrink(wl, tokens):
+    """The last `tokens` query tokens of a one-sequence prefill workload,
+    with the same cache and row lengths (0: the workload unchanged)."""
+    if not tokens or tokens >= wl.T:
+        return wl
+    if wl.B != 1:
+        raise SystemExit("--tokens applies to the prefill workloads only")
+    import dsa_synth as S
+    end = wl.q_pos[-1] + 1
+    return S.prefill_workload(f"prefill_T{tokens}_after{end - tokens}", wl.seed, end - tokens, tokens,
+                              H_I=wl.H_I, H=wl.H, top_k=wl.top_k, hadamard=wl.hadamard)
 
 
 def algorithmic(wl):
@@ -920,7 +936,7 @@ def main():
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0
-    wl = S.config(WORKLOADS[args.workload])
+    wl = shrink(S.config(WORKLOADS[args.workload]), args.tokens)
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     res = measure(dsa, torch, wl, args.steps, args.warmup, args.flush_mb, world=world, e2e_steps=n_e2e,
                   graph=args.graph)
