@@ -41,6 +41,13 @@
  *    1 <= k <= 65536.  Others return DSA_ERR_UNSUPPORTED.
  *  - Device pointers passed to the TMA engine (k_cache, kv_cache, q_lat,
  *    q_rope) must be 16-byte aligned, else DSA_ERR_MISALIGNED.
+ *  - The attention results (out, lse) are written with plain stores and
+ *    never read back, so they may also be pinned host memory that the
+ *    driver maps into the device's address space at the same address
+ *    (cuPointerGetAttribute reports the host address as its device pointer,
+ *    as on NVLink-C2C systems): the result then reaches the host without a
+ *    separate copy.  Whether a pointer is so mapped is the caller's to
+ *    check; the library does not inspect pointers.
  *  - Host validation runs before anything is enqueued; a failing call
  *    enqueues nothing.  A failed launch returns DSA_ERR_CUDA.
  *  - Device-detected problems (a position outside the stated bounds, an

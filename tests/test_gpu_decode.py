@@ -183,3 +183,30 @@ def test_decode_all_scores_tied(dsa):
     assert g["idx"][0].tolist() == list(range(2048))
     assert g["idx"][1].tolist() == list(range(2048))
     assert g["idx"][2].tolist() == list(range(1000)) + [-1] * 1048
+
+
+def test_results_written_into_mapped_pinned_host_memory(dsa):
+    """out and lse may be pinned host memory that the driver maps at the same
+    address: the kernels then write the result there directly.  The result
+    must equal the device-resident run's bit for bit."""
+    import torch
+    import bench
+    wl = S.config(2)
+    inp = S.make_inputs(wl)
+    h_out = torch.full((wl.T, wl.H, 512), float("nan")).pin_memory()
+    h_lse = torch.full((wl.T, wl.H), float("nan")).pin_memory()
+    m_out, m_lse = bench.host_mapped_alias(torch, h_out), bench.host_mapped_alias(torch, h_lse)
+    if m_out is None or m_lse is None:
+        pytest.skip("pinned host memory is not mapped at the same address on this system")
+    b = dev_batch(wl)
+    ws = dsa.workspace(dsa.DSA_OP_DECODE, b, wl.H_I, wl.H, wl.top_k)
+    args = [to_dev(inp.k_new), to_dev(inp.q_idx), to_dev(inp.w), to_dev(inp.q_lat), to_dev(inp.q_rope),
+            to_dev(inp.k_cache), to_dev(inp.kv_cache), b, wl.top_k, wl.sm_scale, wl.hadamard]
+    out = torch.empty((wl.T, wl.H, 512), device="cuda")
+    lse = torch.empty((wl.T, wl.H), device="cuda")
+    idx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device="cuda")
+    dsa.dsa_decode(*args, out, lse, idx, ws)
+    dsa.dsa_decode(*args, m_out, m_lse, idx, ws)        # the append rewrites the same keys
+    torch.cuda.synchronize()
+    assert dsa.dsa_read_device_status(ws) == 0
+    assert torch.equal(h_out, out.cpu()) and torch.equal(h_lse, lse.cpu())
