@@ -338,6 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_s = idesc_f16(kRows, kHeads, true, false, false);
             const uint32_t id_o = idesc_f16(128, kHeads, true, true, true);
             const uint32_t qa = smem_u32(q_s), ca = smem_u32(c_s);
+            // Descriptors differ only in their start address (bits 0..13, in
+            // 16-byte units, no carry: shared addresses are below 256 KB), so
+            // each product adds a constant offset to a base descriptor.
+            const uint64_t s_a0 = sdesc_sw128(ca, 16, 1024), s_b0 = sdesc_sw128(qa, 16, 1024);
+            const uint64_t o_a0 = sdesc_sw128(ca, kCBlockBytes, 1024), o_b0 = sdesc_sw128(ca + 8 * kCBlockBytes,
+                                                                                          kCBlockBytes, 1024);
+            const int s_blocks = p.rope ? kBlocks : kBlocks - 1;
             int s_next = 0, o_next = 0;
             uint64_t t_last = global_ns();
             while (o_next < n_my) {
@@ -346,15 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_test(smem_u32(&ctl.c_full[s_next & 1]), (uint32_t)(s_next >> 1) & 1u)) {
                     const int buf = s_next & 1;
                     tc_fence_after();
-                    const uint32_t cb = ca + buf * kCBytes;
+                    uint64_t ad = s_a0 + (uint64_t)((buf * kCBytes) >> 4), bd = s_b0;
+                    const uint32_t d_s = tmem + kColS + buf * kHeads;
 #pragma unroll 1
-                    for (int kb = 0; kb < (p.rope ? kBlocks : kBlocks - 1); ++kb) {
+                    for (int kb = 0; kb < s_blocks; ++kb) {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ad = sdesc_sw128(cb + kb * kCBlockBytes + ks * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(qa + kb * kQBlockBytes + ks * 32, 16, 1024);
-                            umma_f16(tmem + kColS + buf * kHeads, ad, bd, id_s, (kb | ks) != 0);
-                        }
+                        for (int ks = 0; ks < 4; ++ks)
+                            umma_f16(d_s, ad + (uint64_t)(ks * 2), bd + (uint64_t)(ks * 2), id_s, (kb | ks) != 0);
+                        ad += (uint64_t)(kCBlockBytes >> 4);
+                        bd += (uint64_t)(kQBlockBytes >> 4);
                     }
                     umma_commit(smem_u32(&ctl.s_full[buf]));
                     ++s_next;
@@ -364,14 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_test(smem_u32(&ctl.p_full[o_next & 1]), (uint32_t)(o_next >> 1) & 1u)) {
                     const int buf = o_next & 1;
                     tc_fence_after();
-                    const uint32_t cb = ca + buf * kCBytes;
+                    const uint64_t boff = (uint64_t)((buf * kCBytes) >> 4);
+                    const uint32_t acc0 = o_next > 0 ? 1u : 0u;
+                    uint64_t ad = o_a0 + boff;
+                    const uint64_t bd = o_b0 + boff;
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                        for (int ks = 0; ks < kRows / 16; ++ks) {
-                            const uint64_t ad = sdesc_sw128(cb + (2 * c) * kCBlockBytes + ks * 2048, kCBlockBytes, 1024);
-                            const uint64_t bd = sdesc_sw128(cb + 8 * kCBlockBytes + ks * 2048, kCBlockBytes, 1024);
-                            umma_f16(tmem + kColO + c * kHeads, ad, bd, id_o, (o_next > 0 || ks > 0) ? 1u : 0u);
-                        }
+                        for (int ks = 0; ks < kRows / 16; ++ks)
+                            umma_f16(tmem + kColO + c * kHeads, ad + (uint64_t)(ks * (2048 >> 4)),
+                                     bd + (uint64_t)(ks * (2048 >> 4)), id_o, (acc0 | (uint32_t)ks) ? 1u : 0u);
+                        ad += (uint64_t)((2 * kCBlockBytes) >> 4);
                     }
                     umma_commit(smem_u32(&ctl.c_empty[buf]));
                     umma_commit(smem_u32(&ctl.o_full));
