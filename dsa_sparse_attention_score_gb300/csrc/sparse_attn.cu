@@ -136,18 +136,29 @@ __device__ __forceinline__ void half_reduce_32(const float (&x)[32], int lane, f
 // One producer warp copies 16 rows of a tile (tile rows r0 .. r0 + 15) whose
 // cache rows lanes 0..15 hold in my_row, CPR 16-byte chunks per row (72 with
 // the rope tail, 64 without), into the nine-block SWIZZLE_128B layout the
-// MMAs read.  Instruction j of lane l copies flat chunk 32 j + l of the
-// warp's 16 x CPR chunks, so every warp instruction reads at most two rows'
-// contiguous runs of bytes.
+// MMAs read.  Within each group of four rows, warp instruction i copies flat
+// chunks 32 i .. 32 i + 31, so every warp instruction reads at most two rows'
+// contiguous runs of bytes; the addresses are set up once per i and advance
+// by a constant per group.
 template <int CPR>
 __device__ __forceinline__ void copy_rows16(uint32_t cb, const uint8_t *kv, int32_t my_row, int r0, int lane) {
-#pragma unroll 4
-    for (int j = 0; j < CPR / 2; ++j) {
-        const int f = j * 32 + lane;
-        const int rl = f / CPR, c = f - rl * CPR;
-        const int32_t row = __shfl_sync(0xffffffffu, my_row, rl);
-        const uint32_t dst = cb + (uint32_t)(c >> 3) * kCBlockBytes + sw128_offset((uint32_t)(r0 + rl), (uint32_t)(c & 7));
-        cp_async16(dst, kv + (int64_t)row * (CPR * 16) + c * 16);
+    // Four rows at a time: their 4 * CPR chunks are PER per lane, and lane l's
+    // i-th chunk sits at the same (row in the group, chunk) in every group.
+    // r0 is a multiple of 8, so a row's swizzle phase is (4 g + rg) mod 8:
+    // odd groups flip bit 2 of the chunk index, i.e. bit 6 of the address.
+    constexpr int PER = 4 * CPR / 32;
+    static_assert(4 * CPR % 32 == 0, "a group of four rows is a whole number of warp-wide copies");
+#pragma unroll 1
+    for (int i = 0; i < PER; ++i) {
+        const int f = lane + 32 * i;
+        const int rg = f / CPR, c = f - rg * CPR;
+        const uint32_t d0 = cb + (uint32_t)(c >> 3) * kCBlockBytes + sw128_offset((uint32_t)(r0 + rg), (uint32_t)(c & 7));
+        const uint8_t *src = kv + c * 16;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int32_t row = __shfl_sync(0xffffffffu, my_row, 4 * g + rg);
+            cp_async16((d0 + (uint32_t)g * 512u) ^ ((uint32_t)(g & 1) << 6), src + (int64_t)row * (CPR * 16));
+        }
     }
 }
 
