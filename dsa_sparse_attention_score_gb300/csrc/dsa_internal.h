@@ -163,7 +163,7 @@ cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStre
 
 // Sets a kernel's dynamic shared-memory limit once per device; `slot`
 // (0..kSmemAttrSlots-1) names the kernel instance.
-constexpr int kSmemAttrSlots = 9;
+constexpr int kSmemAttrSlots = 11;
 cudaError_t ensure_smem_attr(const void *func, int slot, size_t bytes);
 
 // Rows of one attention tile (the unit of the split across CTAs).

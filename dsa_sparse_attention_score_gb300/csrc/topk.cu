@@ -578,8 +578,9 @@ cudaError_t launch_cluster(const float *scores, int64_t ld, const DevBatch &b, R
                            int n_sink, const int32_t *sink_pos0) {
     if (nrows * C > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const size_t stage = (size_t)std::min(k, NT * KPT) * 4;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_cluster_kernel<NT, KPT>),
-                                     NT == 256 ? 5 : (KPT == 16 ? 6 : 7), (size_t)NT * KPT * 4);
+    constexpr int slot = NT == 256 ? 5 : KPT == 16 ? 6 : KPT == 32 ? 7 : KPT == 8 ? 9 : 10;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(topk_cluster_kernel<NT, KPT>), slot,
+                                     (size_t)NT * KPT * 4);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nrows * C));
@@ -611,6 +612,12 @@ cudaError_t launch_topk_cfg(const float *scores, int64_t ld, const DevBatch &b, 
     if (nrows <= 0) return cudaSuccess;
     if (C < 1 || C > kMaxCluster || (int64_t)nt * kpt * C < b.max_kv) return cudaErrorInvalidValue;
     const int vec = (ld % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0) ? 1 : 0;
+    if (nt == 512 && kpt == 4)
+        return launch_cluster<512, 4>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec, n_sink,
+                                      sink_pos0);
+    if (nt == 512 && kpt == 8)
+        return launch_cluster<512, 8>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec, n_sink,
+                                      sink_pos0);
     if (nt == 512 && kpt == 16)
         return launch_cluster<512, 16>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, C, vec, n_sink,
                                                    sink_pos0);
@@ -638,7 +645,11 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
     if (n_max <= 8192) {
         if (nrows >= 2 * kSMs)
             return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 256, 32, 1, n_sink, sink_pos0);
-        return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 16, 1, n_sink, sink_pos0);
+        // the smallest register array that holds the row: the per-key loops
+        // run over all KPT slots (measured on GB300, 2048-key pool rows: 512 x 8
+        // instead of 512 x 16 took 2.7 us off the kpool decode top-k)
+        const int kpt = n_max <= 512 * 4 ? 4 : n_max <= 512 * 8 ? 8 : 16;
+        return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, kpt, 1, n_sink, sink_pos0);
     }
     const bool vec = ld % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0;
     const bool cluster_fits = n_max <= (int64_t)kMaxCluster * 512 * 32;
@@ -652,6 +663,13 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const DevBatch &b, RowM
                                                       sink_pos0, 8);
         return launch_stream<512, 768>(scores, ld, b, rows, k, idx, status, stream, pdl, nrows, n_sink, sink_pos0, 0);
     }
+    // up to 65536 keys: clusters of up to 8 CTAs with 16 keys per thread
+    // (measured on GB300, ragged decode rows of 4k-64k keys: 25.1 -> 17.0 us
+    // against 4 CTAs of 32 keys per thread: half the work per thread in every
+    // pass outweighs the wider histogram exchange)
+    if (n_max <= (int64_t)kMaxCluster * 512 * 16)
+        return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 16,
+                               (int)((n_max + 512 * 16 - 1) / (512 * 16)), n_sink, sink_pos0);
     if (cluster_fits)
         return launch_topk_cfg(scores, ld, b, rows, k, idx, status, stream, pdl, 512, 32,
                                (int)((n_max + 512 * 32 - 1) / (512 * 32)), n_sink, sink_pos0);
