@@ -162,6 +162,16 @@ def _topk_case(kind, rng):
         for t, p in enumerate(pos):
             n = p + 1
             s[t, (np.arange(0, 4096, 20) * n) // 4096] = 100.0
+    # few rows of 4097..8192 keys: the one-CTA 16-bit-digit path
+    elif kind == "row16_all_equal":             # every key in one bin: the second 16-bit digit
+        L, pos = 6000, [5999, 4500, 4097]
+        s = np.full((len(pos), L), -0.375, np.float32)
+    elif kind == "row16_mixed":                 # -inf, signed zeros and a run of ties around the threshold
+        L, pos = 7000, [6999, 6000, 5000, 4097]
+        s = rng.standard_normal((len(pos), L)).astype(np.float32)
+        s[:, ::3] = -np.inf
+        s[:, 1::7] = np.where(rng.random((len(pos), len(range(1, L, 7)))) < 0.5, np.float32(0.0), np.float32(-0.0))
+        s[:, 2000:2040] = 0.6745
     elif kind == "narrow":                      # distinct values that share high bits
         L, pos = 9000, [8999]
         s = (1.0 + rng.integers(0, 1 << 12, (1, L)) * 2.0 ** -23).astype(np.float32)
@@ -172,7 +182,7 @@ def _topk_case(kind, rng):
 
 @pytest.mark.parametrize("kind", ["random", "ties", "all_equal", "signed_zero", "neg_inf", "long_row", "narrow",
                                   "cluster3", "cluster5", "cluster7", "beyond_cluster", "beyond_cluster_unaligned",
-                                  "unaligned_cluster5",
+                                  "unaligned_cluster5", "row16_all_equal", "row16_mixed",
                                   "stream_random", "stream_all_equal", "stream_sample_miss"])
 @pytest.mark.parametrize("k", [1, 2048])
 def test_topk_bit_exact_on_oracle_scores(dsa, kind, k):
