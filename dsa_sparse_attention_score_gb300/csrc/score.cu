@@ -313,12 +313,6 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_base), p.tmem_cols);
         tmem_relinquish();
-        if (append_tile >= 0) {
-            const int t = q0 + j_lo;
-            const uint2 kv = appended_key(p.k_new, p.k_dtype, t, p.hadamard_k, lane);
-            reinterpret_cast<uint2 *>(p.k_cache + cache_row(b, seq, kv0, max_p) * D_I)[lane] = kv;   // persist
-            reinterpret_cast<uint2 *>(sm.new_key)[lane] = kv;                        // staging
-        }
     }
     if (warp == 0 && lane == 0) tma_prefetch_desc(&k_map);
     tc_fence_before();
@@ -360,7 +354,15 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer.  It first computes the appended key (its
+        // load and rotation overlap the tile loads the producer has issued).
+        if (append_tile >= 0) {
+            const int t = q0 + j_lo;
+            const uint2 kv = appended_key(p.k_new, p.k_dtype, t, p.hadamard_k, lane);
+            reinterpret_cast<uint2 *>(p.k_cache + cache_row(b, seq, kv0, max_p) * D_I)[lane] = kv;   // persist
+            reinterpret_cast<uint2 *>(sm.new_key)[lane] = kv;                        // staging
+            __syncwarp();
+        }
         if (lane == 0 && wait_bar(smem_u32(&sm.q_ready), 0, sm, p.status, b.wait_ns)) {
             tc_fence_after();
             const uint32_t idesc = idesc_f16(128, p.NP, false, false, false);
