@@ -69,6 +69,7 @@ struct ScoreParams {
     int tiles_per_cta;
     int stages;
     int early;                // trigger dependents at the start (see launch_score)
+    int balance;              // one token per sequence: CTAs shared out by sequence length (see below)
     int groups_per_seq;
     uint32_t tmem_cols;
 };
@@ -87,6 +88,8 @@ struct Smem {
     int64_t meta_kv0;
     int32_t pos[kMaxGroup];
     int64_t out_row[kMaxGroup];
+    uint32_t bal_warp[32];    // balanced chunking: per-warp sums
+    int32_t bal_seq, bal_lo, bal_hi;
 };
 
 // Two halves of 256 columns (a 512-row query operand) leave room for a
@@ -231,11 +234,75 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     if (p.early) pdl_trigger();
 
     // ---- which tokens and keys this CTA covers (uniform across the CTA)
-    const int seq = blockIdx.y / p.groups_per_seq;
-    // later groups of a sequence see more keys: launch them first, so that
-    // the last wave holds the shortest CTAs (measured on GB300, 4096 tokens
-    // after 4096: 3% off the scoring)
-    const int grp = p.groups_per_seq - 1 - (int)(blockIdx.y % p.groups_per_seq);
+    int seq, grp, tile_lo = 0, tile_cnt = p.tiles_per_cta;
+    if (p.balance) {
+        // One token per sequence, at most one sequence per thread: sequence s,
+        // whose token sees n_s key tiles, gets c_s = min(ceil(n_s / 2),
+        // 1 + n_s (G - B) / sum n) of the G CTAs (at most G in all, each with
+        // two tiles or more), CTA j of them the tiles [j n_s / c_s,
+        // (j + 1) n_s / c_s): every CTA streams about the same number of tiles
+        // however the lengths differ.  Every CTA computes the same shares.
+        const int nthreads = (int)blockDim.x, tid = (int)threadIdx.x;
+        const int G = (int)gridDim.x;
+        uint32_t n_s = 0;
+        if (tid < b.B) {
+            // a sequence that gets no CTA is checked here (a sequence may have
+            // no token; pool mode: -1 is an empty row)
+            const int q0 = __ldg(b.cu_q + tid), q1 = __ldg(b.cu_q + tid + 1);
+            bool bad = q0 < 0 || q1 > b.T || q1 < q0 || q1 - q0 > b.max_q;
+            if (!bad && q1 > q0) {
+                const int pos = visible_last(b, q0);
+                if (pos >= 0 && pos < b.max_kv) n_s = (uint32_t)(pos / kTileKeys) + 1u;
+                else bad = !(b.pool_log2 && pos == -1);
+            }
+            if (bad && blockIdx.x == 0) flag(p.status, DSA_DEV_BAD_POSITION);
+        }
+        if (tid == 0) sm.bal_seq = -1;
+        uint32_t v = n_s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) sm.bal_warp[warp] = v;
+        __syncthreads();
+        uint32_t total = 0;
+        for (int w = 0; w < nthreads / 32; ++w) total += sm.bal_warp[w];
+        uint32_t c_s = 0;
+        if (n_s > 0) {
+            const uint64_t share = 1u + (uint64_t)n_s * (uint64_t)(G - b.B) / total;
+            const uint64_t half = (n_s + 1u) / 2u;
+            c_s = (uint32_t)(share < half ? share : half);
+        }
+        uint32_t incl = c_s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        __syncthreads();                                 // the totals above are read
+        if (lane == 31) sm.bal_warp[warp] = incl;
+        __syncthreads();
+        uint32_t pre = incl - c_s;
+        for (int w = 0; w < warp; ++w) pre += sm.bal_warp[w];
+        const uint32_t cta = blockIdx.x;
+        if (c_s > 0 && pre <= cta && cta < pre + c_s) {
+            const uint32_t j = cta - pre;
+            sm.bal_seq = tid;
+            sm.bal_lo = (int)(j * n_s / c_s);
+            sm.bal_hi = (int)((j + 1u) * n_s / c_s);
+        }
+        __syncthreads();
+        if (sm.bal_seq < 0) return;                      // more CTAs than shares
+        seq = sm.bal_seq;
+        grp = 0;
+        tile_lo = sm.bal_lo;
+        tile_cnt = sm.bal_hi - sm.bal_lo;
+        __syncthreads();                                 // sm.meta_* are written next
+    } else {
+        seq = blockIdx.y / p.groups_per_seq;
+        // later groups of a sequence see more keys: launch them first, so that
+        // the last wave holds the shortest CTAs (measured on GB300, 4096 tokens
+        // after 4096: 3% off the scoring)
+        grp = p.groups_per_seq - 1 - (int)(blockIdx.y % p.groups_per_seq);
+    }
     if (seq >= b.B) return;
     if (threadIdx.x == 0) {                       // three independent loads
         sm.meta_q0 = __ldg(b.cu_q + seq);
@@ -275,14 +342,14 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     __syncthreads();
     int max_p = -1;
     for (int i = 0; i < g; ++i) max_p = max(max_p, sm.pos[i]);
-    const int64_t chunk0 = (int64_t)blockIdx.x * p.tiles_per_cta * kTileKeys;
+    const int64_t chunk0 = p.balance ? (int64_t)tile_lo * kTileKeys : (int64_t)blockIdx.x * p.tiles_per_cta * kTileKeys;
     int n_mma = 0;
     if (max_p >= chunk0)
-        n_mma = (int)min((int64_t)p.tiles_per_cta, (max_p - chunk0) / kTileKeys + 1);
+        n_mma = (int)min((int64_t)tile_cnt, (max_p - chunk0) / kTileKeys + 1);
     int n_tiles = n_mma;
     if (p.fill_masked) {
         const int64_t left = p.ld - chunk0;
-        n_tiles = left <= 0 ? 0 : (int)min((int64_t)p.tiles_per_cta, (left + kTileKeys - 1) / kTileKeys);
+        n_tiles = left <= 0 ? 0 : (int)min((int64_t)tile_cnt, (left + kTileKeys - 1) / kTileKeys);
         n_tiles = max(n_tiles, n_mma);
     }
     if (n_tiles == 0) return;
@@ -290,11 +357,11 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     // (just appended) key depends on the preceding kernel; otherwise all do.
     int first_dependent = n_mma;
     if (p.depends == 2 || (p.depends == 1 && n_seq > 1)) first_dependent = 0;
-    else if (p.depends == 1 && n_mma > 0 && (max_p - chunk0) / kTileKeys < p.tiles_per_cta)
+    else if (p.depends == 1 && n_mma > 0 && (max_p - chunk0) / kTileKeys < tile_cnt)
         first_dependent = n_mma - 1;
     // Fused append: this CTA holds the tile of the token's own position.
     const int append_tile = (p.fuse_append && n_seq == 1 && n_mma > 0 &&
-                             (max_p - chunk0) / kTileKeys < p.tiles_per_cta) ? n_mma - 1 : -1;
+                             (max_p - chunk0) / kTileKeys < tile_cnt) ? n_mma - 1 : -1;
 
     // ---- set-up
     if (threadIdx.x == 0) {
@@ -605,9 +672,23 @@ cudaError_t launch_score(const ScoreLaunch &a, const CUtensorMap &k_map, const D
     // per SM.
     p.stages = (p.G == 1 || tpc <= 2) ? 2 : kMaxStages;
     while (p.stages > 2 && score_smem_bytes(p.NQ, p.hadamard_q, p.stages) > kSmemLimit) --p.stages;
-    const int64_t chunks = (tiles + tpc - 1) / tpc;
-    const int64_t groups = (int64_t)b.B * p.groups_per_seq;
+    int64_t chunks = (tiles + tpc - 1) / tpc;
+    int64_t groups = (int64_t)b.B * p.groups_per_seq;
     if (groups > 65535 || chunks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    // One token per sequence (decode) with long rows (chunks of more than two
+    // tiles): a grid of one wave (two CTAs per SM) whose CTAs share the
+    // sequences' tiles out by length on the device, so that ragged batches do
+    // not leave a few SMs streaming the longest sequences (see the kernel;
+    // measured on GB300, 32 sequences of 4k-64k keys: 75.1 -> 57.1 us).  With
+    // short rows the fixed chunks are already even and the shares' extra
+    // round trip would cost more (8 x 8192 keys: 8.8 -> 10.6 us).  Shares
+    // need one sequence per thread.
+    p.balance = (p.G == 1 && b.max_q == 1 && !a.fill_masked && tpc > 2 && b.B <= ScoreCfg<4>::kThreads &&
+                 b.B < kSMs) ? 1 : 0;
+    if (p.balance) {
+        chunks = 2 * kSMs;
+        groups = 1;
+    }
 
     const size_t smem = score_smem_bytes(p.NQ, p.hadamard_q, p.stages);
     if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;

@@ -185,6 +185,25 @@ def test_decode_all_scores_tied(dsa):
     assert g["idx"][2].tolist() == list(range(1000)) + [-1] * 1048
 
 
+def test_decode_with_tokenless_sequences(dsa):
+    """Sequences with no query token this step (cu_q[b + 1] == cu_q[b]) in
+    the middle and at the end of a batch of long rows, whose score CTAs are
+    shared out by sequence length: the empty sequences get no CTA and raise
+    no status."""
+    wl = S.Workload("decode_gaps", 63, kv_len=[30000, 9000, 50000, 4000, 20000, 7000],
+                    q_pos=[29999, 49000, 19990], cu_q=[0, 1, 1, 2, 2, 3, 3], H_I=16, H=8, top_k=2048)
+    check_workload(dsa, wl)
+
+
+def test_decode_many_ragged_sequences(dsa):
+    """120 sequences of 1k-16k keys: the length-proportional shares of the
+    score grid range from one CTA to the cap of two tiles per CTA."""
+    kv_len = S.ragged_lengths(64, 120, lo=1000, hi=16000)
+    kv_len[7], kv_len[50] = 16000, 129
+    wl = S.decode_workload("decode_many", 64, kv_len, H_I=16, H=8, top_k=512)
+    check_workload(dsa, wl)
+
+
 def test_results_written_into_mapped_pinned_host_memory(dsa):
     """out and lse may be pinned host memory that the driver maps at the same
     address: the kernels then write the result there directly.  The result
