@@ -86,6 +86,7 @@ struct Smem {
     int32_t abort_flag;
     int32_t meta_q0, meta_q1, meta_max_p;
     int64_t meta_kv0;
+    int32_t spec_tok, spec_pos;   // a token whose stored position is already loaded (-1: none)
     int32_t pos[kMaxGroup];
     int64_t out_row[kMaxGroup];
     uint32_t bal_warp[32];    // balanced chunking: per-warp sums
@@ -232,9 +233,50 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     const DevBatch &b = p.b;
     tl_start(b.timeline, kTlScore);
     if (p.early) pdl_trigger();
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&k_map);   // fetched while the batch data loads
 
-    // ---- which tokens and keys this CTA covers (uniform across the CTA)
+    // Barriers and tensor memory.  Balanced decode grids set up while their
+    // batch loads are in flight; the others once the positions are known:
+    // on GB300 (batched decode, 8 x 8192 keys, cold L2) allocating the tensor
+    // memory at the start made this kernel 0.7 us faster but left the
+    // attention kernel that follows 5-6 us slower, for a reason not found.
+    auto set_up = [&]() {
+        if (threadIdx.x == 64) {
+            for (int s = 0; s < n_stages; ++s) {
+                mbar_init(smem_u32(&sm.full[s]), 1);
+                mbar_init(smem_u32(&sm.empty[s]), 1);
+            }
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(smem_u32(&sm.acc_full[s]), 1);
+                mbar_init(smem_u32(&sm.acc_empty[s]), kEpiWarps);
+            }
+            mbar_init(smem_u32(&sm.q_ready), kEpiWarps);
+            sm.abort_flag = 0;
+            fence_mbar_init();
+        }
+        if (warp == 1) {
+            tmem_alloc(smem_u32(&sm.tmem_base), p.tmem_cols);
+            tmem_relinquish();
+        }
+    };
+    // Every return after the set-up gives the tensor memory back.
+    bool have_tmem = false;
+    auto release = [&](uint32_t tm) {
+        if (have_tmem && warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tm, p.tmem_cols);
+        }
+    };
+    // The last visible position of a token from its stored position.
+    auto visible = [&](int q) { return b.pool_log2 ? ((q + 1) >> b.pool_log2) - 1 : q; };
+
+    // ---- which tokens and keys this CTA covers (uniform across the CTA).
+    // One-token groups (decode) load their token's position in the same round
+    // trip as the batch offsets, on the guess that sequence s's token is
+    // token s (every sequence has exactly one); the guess is checked, and a
+    // wrong one costs a second load.
     int seq, grp, tile_lo = 0, tile_cnt = p.tiles_per_cta;
+    uint32_t tmem;
     if (p.balance) {
         // One token per sequence, at most one sequence per thread: sequence s,
         // whose token sees n_s key tiles, gets c_s = min(ceil(n_s / 2),
@@ -245,13 +287,23 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         const int nthreads = (int)blockDim.x, tid = (int)threadIdx.x;
         const int G = (int)gridDim.x;
         uint32_t n_s = 0;
+        int my_q0 = 0, my_q1 = 0, my_raw = -1;
+        int64_t my_kv = 0;
+        int guess = -1;
+        if (tid < b.B) {
+            my_q0 = __ldg(b.cu_q + tid);
+            my_q1 = __ldg(b.cu_q + tid + 1);
+            guess = __ldg(b.q_pos + min(tid, b.T - 1));
+            my_kv = seq_base(b, tid);
+        }
+        set_up();
         if (tid < b.B) {
             // a sequence that gets no CTA is checked here (a sequence may have
             // no token; pool mode: -1 is an empty row)
-            const int q0 = __ldg(b.cu_q + tid), q1 = __ldg(b.cu_q + tid + 1);
-            bool bad = q0 < 0 || q1 > b.T || q1 < q0 || q1 - q0 > b.max_q;
-            if (!bad && q1 > q0) {
-                const int pos = visible_last(b, q0);
+            bool bad = my_q0 < 0 || my_q1 > b.T || my_q1 < my_q0 || my_q1 - my_q0 > b.max_q;
+            if (!bad && my_q1 > my_q0) {
+                my_raw = my_q0 == tid ? guess : __ldg(b.q_pos + my_q0);
+                const int pos = visible(my_raw);
                 if (pos >= 0 && pos < b.max_kv) n_s = (uint32_t)(pos / kTileKeys) + 1u;
                 else bad = !(b.pool_log2 && pos == -1);
             }
@@ -262,7 +314,11 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) sm.bal_warp[warp] = v;
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
+        tmem = sm.tmem_base;
+        have_tmem = true;
         uint32_t total = 0;
         for (int w = 0; w < nthreads / 32; ++w) total += sm.bal_warp[w];
         uint32_t c_s = 0;
@@ -284,51 +340,71 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         for (int w = 0; w < warp; ++w) pre += sm.bal_warp[w];
         const uint32_t cta = blockIdx.x;
         if (c_s > 0 && pre <= cta && cta < pre + c_s) {
+            // the owning thread knows the sequence's offsets and position
             const uint32_t j = cta - pre;
             sm.bal_seq = tid;
             sm.bal_lo = (int)(j * n_s / c_s);
             sm.bal_hi = (int)((j + 1u) * n_s / c_s);
+            sm.meta_q0 = my_q0;
+            sm.meta_q1 = my_q1;
+            sm.meta_kv0 = my_kv;
+            sm.spec_tok = my_q0;
+            sm.spec_pos = my_raw;
         }
         __syncthreads();
-        if (sm.bal_seq < 0) return;                      // more CTAs than shares
+        if (sm.bal_seq < 0) {                            // more CTAs than shares
+            release(tmem);
+            return;
+        }
         seq = sm.bal_seq;
         grp = 0;
         tile_lo = sm.bal_lo;
         tile_cnt = sm.bal_hi - sm.bal_lo;
-        __syncthreads();                                 // sm.meta_* are written next
     } else {
         seq = blockIdx.y / p.groups_per_seq;
         // later groups of a sequence see more keys: launch them first, so that
         // the last wave holds the shortest CTAs (measured on GB300, 4096 tokens
         // after 4096: 3% off the scoring)
         grp = p.groups_per_seq - 1 - (int)(blockIdx.y % p.groups_per_seq);
+        if (seq >= b.B) return;
+        if (threadIdx.x == 0) {                   // independent loads, one round trip
+            const int q0 = __ldg(b.cu_q + seq);
+            const int q1 = __ldg(b.cu_q + seq + 1);
+            const int64_t kv0 = seq_base(b, seq);
+            const bool guess = p.G == 1 && seq < b.T;
+            const int gp = guess ? __ldg(b.q_pos + seq) : -1;
+            sm.meta_q0 = q0;
+            sm.meta_q1 = q1;
+            sm.meta_kv0 = kv0;
+            sm.spec_tok = guess ? seq : -1;
+            sm.spec_pos = gp;
+        }
+        __syncthreads();
+        tmem = 0;
     }
-    if (seq >= b.B) return;
-    if (threadIdx.x == 0) {                       // three independent loads
-        sm.meta_q0 = __ldg(b.cu_q + seq);
-        sm.meta_q1 = __ldg(b.cu_q + seq + 1);
-        sm.meta_kv0 = seq_base(b, seq);
-    }
-    __syncthreads();
     const int q0 = sm.meta_q0, q1 = sm.meta_q1;
     const int64_t kv0 = sm.meta_kv0;
     const int n_seq = q1 - q0;
     if (q0 < 0 || q1 > b.T || n_seq < 0 || n_seq > b.max_q) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && grp == 0) flag(p.status, DSA_DEV_BAD_POSITION);
+        release(tmem);
         return;
     }
     const int win_lo = p.rows.slab ? p.rows.j0 : 0;
     const int win_hi = p.rows.slab ? min(p.rows.j0 + p.rows.J, n_seq) : n_seq;
     const int j_lo = win_lo + grp * p.G;
     const int j_hi = min(j_lo + p.G, win_hi);
-    if (j_lo >= j_hi) return;
+    if (j_lo >= j_hi) {
+        release(tmem);
+        return;
+    }
     const int g = j_hi - j_lo;
     const int tph = p.G / p.halves;               // tokens per half
     const int hv = (p.halves == 2 && g > tph) ? 2 : 1;   // MMA steps per tile
     if ((int)threadIdx.x < g) {                   // the group's positions, in parallel
         const int i = threadIdx.x;
         const int t = q0 + j_lo + i;
-        const int pos = visible_last(b, t);          // a pool index in pool mode
+        const int pos = visible(t == sm.spec_tok ? sm.spec_pos : __ldg(b.q_pos + t));   // a pool index in pool mode
         bool ok = pos >= 0 && pos < b.max_kv && kv0 >= 0;
         if (ok) {
             const int64_t row = cache_row(b, seq, kv0, pos);
@@ -340,6 +416,14 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         sm.out_row[i] = p.rows.slab ? (int64_t)seq * p.rows.J + (j_lo + i - p.rows.j0) : (int64_t)t;
     }
     __syncthreads();
+    if (!p.balance) {
+        set_up();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tmem = sm.tmem_base;
+        have_tmem = true;
+    }
     int max_p = -1;
     for (int i = 0; i < g; ++i) max_p = max(max_p, sm.pos[i]);
     const int64_t chunk0 = p.balance ? (int64_t)tile_lo * kTileKeys : (int64_t)blockIdx.x * p.tiles_per_cta * kTileKeys;
@@ -352,7 +436,10 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
         n_tiles = left <= 0 ? 0 : (int)min((int64_t)tile_cnt, (left + kTileKeys - 1) / kTileKeys);
         n_tiles = max(n_tiles, n_mma);
     }
-    if (n_tiles == 0) return;
+    if (n_tiles == 0) {
+        release(tmem);
+        return;
+    }
     // With a single query token in the sequence, only the tile holding its own
     // (just appended) key depends on the preceding kernel; otherwise all do.
     int first_dependent = n_mma;
@@ -362,30 +449,6 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     // Fused append: this CTA holds the tile of the token's own position.
     const int append_tile = (p.fuse_append && n_seq == 1 && n_mma > 0 &&
                              (max_p - chunk0) / kTileKeys < tile_cnt) ? n_mma - 1 : -1;
-
-    // ---- set-up
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < n_stages; ++s) {
-            mbar_init(smem_u32(&sm.full[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&sm.acc_full[s]), 1);
-            mbar_init(smem_u32(&sm.acc_empty[s]), kEpiWarps);
-        }
-        mbar_init(smem_u32(&sm.q_ready), kEpiWarps);
-        sm.abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(&sm.tmem_base), p.tmem_cols);
-        tmem_relinquish();
-    }
-    if (warp == 0 && lane == 0) tma_prefetch_desc(&k_map);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
         // ---------------- TMA producer (issues nothing under the failure-path
@@ -430,8 +493,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
             reinterpret_cast<uint2 *>(sm.new_key)[lane] = kv;                        // staging
             __syncwarp();
         }
-        if (lane == 0 && wait_bar(smem_u32(&sm.q_ready), 0, sm, p.status, b.wait_ns)) {
-            tc_fence_after();
+        if (lane == 0) {
             const uint32_t idesc = idesc_f16(128, p.NP, false, false, false);
             const uint32_t qh = smem_u32(q_hi), ql = smem_u32(q_lo);
             const uint32_t qblk = (uint32_t)p.NQ * 128u;
@@ -461,6 +523,19 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
                 fence_proxy_async_smem();
             };
             if constexpr (kEpi == 4) {
+                // Decode CTAs run one or two tiles, so the issue path would
+                // first be fetched into the instruction cache when the first
+                // tile has landed (measured on GB300 after an L2 flush: 2.2 us
+                // from tile to issued products, 0.5 us for the second tile).
+                // Issue it once now on whatever the buffers hold: the first
+                // product of the real step does not accumulate, so it
+                // overwrites this result, and nothing reads the accumulator
+                // before that step's commit.
+            }
+            if (!wait_bar(smem_u32(&sm.q_ready), 0, sm, p.status, b.wait_ns)) {
+                // the loops below are skipped
+            } else if constexpr (kEpi == 4) {
+                tc_fence_after();
                 // one token: one step per tile, the stage released before the
                 // accumulator is signalled (measured on GB300, ragged
                 // long-context decode: 7 us per step faster than the general loop)
@@ -478,6 +553,7 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
                     umma_commit(smem_u32(&sm.acc_full[buf]));
                 }
             } else {
+                tc_fence_after();
                 for (int i = 0; i < n_mma; ++i) {
                     const int s = i % n_stages;
                     const uint32_t k = (uint32_t)(i / n_stages);
@@ -505,14 +581,16 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
     } else {
         // ---------------- query staging + epilogue
         const int ew = warp - 2;  // 0..kEpiWarps-1
-        // stage weights
-        for (int i = threadIdx.x - 64; i < p.NQ; i += 32 * kEpiWarps) {
+        // head weights: this thread's first one is loaded beside the first
+        // query rows (one round trip for both), the rest (none for the
+        // shapes launched: NQ <= 32 kEpiWarps) after them
+        auto weight_at = [&](int i) -> float {
             const int tok = i / p.HP, h = i % p.HP;
-            float wv = 0.f;
-            if (tok < g && h < p.H_I && sm.pos[tok] >= 0)
-                wv = __ldg(p.w + (int64_t)(q0 + j_lo + tok) * p.H_I + h);
-            reinterpret_cast<float *>(sm.w4)[i] = wv;
-        }
+            return (tok < g && h < p.H_I && sm.pos[tok] >= 0) ? __ldg(p.w + (int64_t)(q0 + j_lo + tok) * p.H_I + h)
+                                                                : 0.f;
+        };
+        const int wi0 = (int)threadIdx.x - 64;
+        const float w0 = wi0 < p.NQ ? weight_at(wi0) : 0.f;
         // stage query rows n = tok*HP + h; each warp keeps 8 row loads in flight
         for (int n0 = ew; n0 < p.NQ; n0 += 8 * kEpiWarps) {
             uint2 x[8];
@@ -530,6 +608,8 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
                 if (n < p.NQ) store_q_row(x[u], p.hadamard_q, q_hi, q_lo, p.NQ, n, lane);
             }
         }
+        if (wi0 < p.NQ) reinterpret_cast<float *>(sm.w4)[wi0] = w0;
+        for (int i = wi0 + 32 * kEpiWarps; i < p.NQ; i += 32 * kEpiWarps) reinterpret_cast<float *>(sm.w4)[i] = weight_at(i);
         fence_proxy_async_smem();
         named_barrier(1, 32 * kEpiWarps);     // weights and positions visible to all epilogue warps
         __syncwarp();
