@@ -28,9 +28,10 @@
 // warps gather tile i+1 while the tensor core and the softmax warps work on
 // tile i; the MMA warp issues S^T and O^T products as their inputs arrive,
 // so the softmax of one tile overlaps the score product of the next.  Softmax
-// runs in four warps; an M=64 accumulator puts row m in TMEM lane
-// 32 (m / 16) + m % 16, so lanes 0..15 of each warp quarter hold 16 key rows,
-// read by the two halves of the warp for heads 0..31 and 32..63.
+// runs in eight warps; an M=64 accumulator puts row m in TMEM lane
+// 32 (m / 16) + m % 16, so lanes 0..15 of each lane quarter hold 16 key rows,
+// read by the two warps of the quarter (heads 0..31 and 32..63), each warp's
+// two halves taking 16 heads.
 // The per-head running maximum is only raised when a tile exceeds it by more
 // than 2^8 (lazy rescale of the TMEM accumulator); the final normalisation
 // makes the result exact either way.  With several splits per token, each
@@ -52,9 +53,10 @@ constexpr int kCBlockBytes = kRows * 128;     // 8 KB
 constexpr int kQBytes = kBlocks * kQBlockBytes;
 constexpr int kCBytes = kBlocks * kCBlockBytes;   // one tile buffer
 constexpr int kBufs = 2;
-constexpr int kSoftmaxWarps = 4;              // warps 0..3
-constexpr int kMmaWarp = 4;
-constexpr int kProducerWarps = 4;             // warps 5..8
+constexpr int kSoftmaxWarps = 8;              // warps 0..7: two per TMEM lane quarter
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarps = 4;             // warps 9..12
 constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProducerWarps);
 constexpr int kProducers = 32 * kProducerWarps;
 constexpr float kRescaleLog2 = 8.0f;
@@ -95,7 +97,7 @@ struct Ctl {
     int32_t resc[2];         // any head of warp 0 / 1 rescaled in this tile
     float l[kHeads];
     float inv_l[kHeads];     // 1 / l (0 for an empty row)
-    int32_t warp_alive[4];
+    int32_t warp_alive[kSoftmaxWarps];
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl &c, uint32_t *status,
@@ -108,29 +110,28 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl &c, 
 }
 
 // Transposing butterfly reduction across each 16-lane half of a warp, whose
-// lanes hold the values of 32 consecutive heads (lanes 0..15: heads 0..31,
-// lanes 16..31: heads 32..63): lane L ends up with the reduction over its
-// half of heads 2L and 2L+1.
+// lanes hold 16 values each (lanes 0..15: heads 0..15, lanes 16..31: heads
+// 16..31 of the warp's 32): lane L ends up with the reduction over its half
+// of head L.
 template <bool kMax>
-__device__ __forceinline__ void half_reduce_32(const float (&x)[32], int lane, float &r0, float &r1) {
-    float a[32];
+__device__ __forceinline__ float half_reduce_16(const float (&x)[16], int lane) {
+    float a[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) a[i] = x[i];
+    for (int i = 0; i < 16; ++i) a[i] = x[i];
 #pragma unroll
-    for (int half = 16, bit = 8; half >= 2; half >>= 1, bit >>= 1) {
-        const bool up = lane & bit;
+    for (int half = 8; half >= 1; half >>= 1) {
+        const bool up = lane & half;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             if (i < half) {
                 const float keep = up ? a[half + i] : a[i];
                 const float send = up ? a[i] : a[half + i];
-                const float o = __shfl_xor_sync(0xffffffffu, send, bit);
+                const float o = __shfl_xor_sync(0xffffffffu, send, half);
                 a[i] = kMax ? fmaxf(keep, o) : keep + o;
             }
         }
     }
-    r0 = a[0];
-    r1 = a[1];
+    return a[0];
 }
 
 // One producer warp copies 16 rows of a tile (tile rows r0 .. r0 + 15) whose
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int split = blockIdx.y;
     if (t >= b.T) return;
     // this CTA's slice of the split partials
-    const int64_t part = ((int64_t)t * p.n_split + split) * p.groups + hg;
+    const int64_t part_idx = ((int64_t)t * p.n_split + split) * p.groups + hg;
     tl_start(b.timeline, kTlAttn);
     const int pos = __ldg(b.q_pos + t);
     const int seq = seq_of_warp(b.cu_q, b.B, t, lane);
@@ -198,9 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Empty contribution.
         if (p.n_split > 1) {
             for (int i = threadIdx.x; i < kHeads * D_L / 2; i += kThreads)
-                reinterpret_cast<uint32_t *>(p.part_o + part * kHeads * D_L)[i] = 0u;
+                reinterpret_cast<uint32_t *>(p.part_o + part_idx * kHeads * D_L)[i] = 0u;
             if (threadIdx.x < kHeads) {
-                float *ml = p.part_ml + (part * kHeads + threadIdx.x) * 2;
+                float *ml = p.part_ml + (part_idx * kHeads + threadIdx.x) * 2;
                 ml[0] = -INFINITY;
                 ml[1] = 0.f;
             }
@@ -411,22 +412,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- softmax and epilogue (warps 0..3)
-        const int tx = (int)threadIdx.x;                   // 0..127
-        const int quarter = warp;                          // TMEM lanes 32*warp .. 32*warp+31
-        const int sw = warp;
+        // ---------------- softmax and epilogue (warps 0..7)
+        const int tx = (int)threadIdx.x;                   // 0..255
+        const int quarter = warp & 3;                      // TMEM lanes 32*quarter .. 32*quarter+31
+        const int part = warp >> 2;                        // heads 32*part .. 32*part+31
         // An M=64 accumulator keeps rows in lanes 0..15 of each quarter; the
-        // two halves of the warp read the same 16 rows, heads 0..31 and 32..63.
-        const int hb = 32 * (lane >> 4);                   // this thread's first head
+        // two halves of the warp read the same 16 rows, 16 heads each.
+        const int hb = 32 * part + 16 * (lane >> 4);       // this thread's first head
+        const int hl = 32 * part + lane;                   // the head this lane reduces
         const int r = quarter * 16 + (lane & 15);          // row within the tile
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         if (tx < kHeads) ctl.m[tx] = -INFINITY;
         pdl_wait();
         bool alive = true;
-        named_barrier(1, 128);
-        float lpart[32];
+        named_barrier(1, kSoftmaxThreads);
+        float lpart[16];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) lpart[h] = 0.f;
+        for (int h = 0; h < 16; ++h) lpart[h] = 0.f;
         // Every softmax thread runs the same sequence of named barriers whatever
         // happens; `alive` (warp-uniform) only gates tensor-memory and shared
         // memory work after a bounded wait gave up.
@@ -437,24 +439,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = v >= 0 && v <= pos;
             if (alive) alive = wait_bar(smem_u32(&ctl.s_full[buf]), (uint32_t)(it >> 1) & 1u, ctl, p.status, b.wait_ns);
             alive = __all_sync(0xffffffffu, alive);
-            float x[32];
+            float x[16];
             if (alive) {
                 tc_fence_after();
-                uint32_t u[32];
-                tmem_ld16x2_32(tmem + lane_addr + kColS + buf * kHeads, u);
+                uint32_t u[16];
+                tmem_ld16x2_16(tmem + lane_addr + kColS + buf * kHeads + 32 * part, u);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * p.scale_log2 : -INFINITY;
+                for (int h = 0; h < 16; ++h) x[h] = valid ? __uint_as_float(u[h]) * p.scale_log2 : -INFINITY;
             } else {
 #pragma unroll
-                for (int h = 0; h < 32; ++h) x[h] = -INFINITY;
+                for (int h = 0; h < 16; ++h) x[h] = -INFINITY;
             }
-            // per-head tile maximum across the 64 rows: lane L gets heads 2L, 2L+1
-            float m0, m1;
-            half_reduce_32<true>(x, lane, m0, m1);
-            ctl.red[sw][2 * lane] = m0;
-            ctl.red[sw][2 * lane + 1] = m1;
-            named_barrier(1, 128);
+            // per-head tile maximum across the 64 rows: lane L gets head 32 part + L
+            ctl.red[quarter][hl] = half_reduce_16<true>(x, lane);
+            named_barrier(1, kSoftmaxThreads);
             if (tx < kHeads) {
                 const int h = tx;
                 const float tmax = fmaxf(fmaxf(ctl.red[0][h], ctl.red[1][h]), fmaxf(ctl.red[2][h], ctl.red[3][h]));
@@ -470,11 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool any = __any_sync(0xffffffffu, al != 1.f);
                 if (lane == 0) ctl.resc[warp] = any ? 1 : 0;
             }
-            named_barrier(1, 128);
+            named_barrier(1, kSoftmaxThreads);
             const bool rescale = ctl.resc[0] | ctl.resc[1];   // identical in every thread
-            uint32_t pk[16];
+            uint32_t pk[8];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
+            for (int j = 0; j < 16; j += 2) {
                 const int h = hb + j;
                 const float2 a0 = ctl.ma[h], a1 = ctl.ma[h + 1];
                 const float p0 = (a0.x == -INFINITY) ? 0.f : exp2f(x[j] - a0.x);
@@ -486,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (alive) {
                 // P^T row r into the (now dead) rope block, MN-major SW128: 64
-                // heads = 128 bytes, this thread's 32 heads = chunks hb/8 .. +3.
+                // heads = 128 bytes, this thread's 16 heads = chunks hb/8, hb/8 + 1.
                 uint8_t *prow = c_s + buf * kCBytes + 8 * kCBlockBytes;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 2; ++j) {
                     uint4 q4;
                     q4.x = pk[4 * j]; q4.y = pk[4 * j + 1]; q4.z = pk[4 * j + 2]; q4.w = pk[4 * j + 3];
                     *reinterpret_cast<uint4 *>(prow + sw128_offset((uint32_t)r, (uint32_t)(hb / 8 + j))) = q4;
@@ -498,23 +497,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rescale && it > 0) {
                 // Heads whose maximum moved: rescale their O^T columns once the
                 // previous tile's PV product has landed.  O^T is an M=128
-                // accumulator: every lane of the warp owns one output dim.
+                // accumulator: every lane of the warp owns one output dim; the
+                // two warps of a quarter take 32 heads each.
                 if (alive) alive = wait_bar(smem_u32(&ctl.o_full), (uint32_t)(it - 1) & 1u, ctl, p.status, b.wait_ns);
                 alive = __all_sync(0xffffffffu, alive);
                 if (alive) {
                     tc_fence_after();
-                    for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+                    for (int cq = 0; cq < 8; ++cq) {             // 4 dim blocks x 2 groups of 16 heads
+                        uint32_t u[16];
+                        const int hq = part * 32 + (cq & 1) * 16;
+                        const uint32_t addr = tmem + lane_addr + kColO + (cq >> 1) * kHeads + hq;
+                        tmem_ld16(addr, u);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t u[32];
-                            const uint32_t addr = tmem + lane_addr + kColO + c * kHeads + half * 32;
-                            tmem_ld32(addr, u);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                u[j] = __float_as_uint(__uint_as_float(u[j]) * ctl.alpha[half * 32 + j]);
-                            tmem_st32(addr, u);
-                        }
+                        for (int j = 0; j < 16; ++j)
+                            u[j] = __float_as_uint(__uint_as_float(u[j]) * ctl.alpha[hq + j]);
+                        tmem_st16(addr, u);
                     }
                     tmem_wait_st();
                 }
@@ -527,25 +526,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- final: O^T of the last tile, row sums, outputs
         if (alive) alive = wait_bar(smem_u32(&ctl.o_full), (uint32_t)(n_my - 1) & 1u, ctl, p.status, b.wait_ns);
         alive = __all_sync(0xffffffffu, alive);
-        float l0, l1;
-        half_reduce_32<false>(lpart, lane, l0, l1);
-        ctl.red[sw][2 * lane] = l0;
-        ctl.red[sw][2 * lane + 1] = l1;
-        named_barrier(1, 128);
+        ctl.red[quarter][hl] = half_reduce_16<false>(lpart, lane);
+        named_barrier(1, kSoftmaxThreads);
         if (tx < kHeads) {
             const float l = ctl.red[0][tx] + ctl.red[1][tx] + ctl.red[2][tx] + ctl.red[3][tx];
             ctl.l[tx] = l;
             ctl.inv_l[tx] = l > 0.f ? 1.f / l : 0.f;
         }
-        if (lane == 0) ctl.warp_alive[sw] = alive ? 1 : 0;
-        named_barrier(1, 128);
-        const bool all_alive = ctl.warp_alive[0] && ctl.warp_alive[1] && ctl.warp_alive[2] && ctl.warp_alive[3];
+        if (lane == 0) ctl.warp_alive[warp] = alive ? 1 : 0;
+        named_barrier(1, kSoftmaxThreads);
+        bool all_alive = true;
+#pragma unroll
+        for (int w = 0; w < kSoftmaxWarps; ++w) all_alive = all_alive && ctl.warp_alive[w];
         if (all_alive) {
             // This CTA's [head][dim] block straight from TMEM: thread (quarter,
             // lane) holds output dim c*128 + quarter*32 + lane of every head,
-            // so each warp store writes one head's contiguous run of dims.  The
-            // output (one split) is normalised and float32; a split's partial
-            // is unnormalised bf16 (measured on GB300, batched decode: the
+            // so each warp store writes one head's contiguous run of dims; the
+            // two warps of a quarter store 32 heads each.  The output (one
+            // split) is normalised and float32; a split's partial is
+            // unnormalised bf16 (measured on GB300, batched decode: the
             // per-element 1 / l multiply there cost 3.6 us per CTA, pairing
             // lanes for 4-byte stores 0.9 us).
             tc_fence_after();
@@ -556,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // accumulator columns of each 128-dim block
                 float *dst = p.out + ((int64_t)t * H + h0) * D_L;
 #pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 2 * part; q < 2 * part + 2; ++q) {
                     float inv[16];
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) inv[jj] = ctl.inv_l[q * 16 + jj];
@@ -574,25 +573,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                uint16_t *dst = p.part_o + part * kHeads * D_L;
+                uint16_t *dst = p.part_o + part_idx * kHeads * D_L;
                 for (int c = 0; c < 4; ++c) {
                     const int d = c * 128 + rd;
+                    uint32_t u[32];
+                    tmem_ld32(tmem + lane_addr + kColO + c * kHeads + part * 32, u);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t u[32];
-                        tmem_ld32(tmem + lane_addr + kColO + c * kHeads + half * 32, u);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj)
-                            dst[(half * 32 + jj) * D_L + d] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[jj])));
-                    }
+                    for (int jj = 0; jj < 32; ++jj)
+                        dst[(part * 32 + jj) * D_L + d] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[jj])));
                 }
             }
             if (tx < kHeads) {
                 const int h = tx;
                 const float l = ctl.l[h], m = ctl.m[h];
                 if (p.n_split > 1) {
-                    float *ml = p.part_ml + (part * kHeads + h) * 2;
+                    float *ml = p.part_ml + (part_idx * kHeads + h) * 2;
                     ml[0] = l > 0.f ? m : -INFINITY;
                     ml[1] = l;
                 } else if (p.lse && h < nh) {
