@@ -25,23 +25,24 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
 std::mutex g_setup_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+void *g_scratch_ptr[kMaxDevices] = {};   // the address whose status block was last cleared
 
-// Device address of the scratch array on the current device, found (and its
-// status block cleared) on the first call made with that device current.
+// Device address of the scratch array on the current device, looked up on
+// every call (a device reset reloads the module, and the array may move);
+// its status block is cleared whenever the address is new.
 dsa_status_t scratch_for_current_device(cudaStream_t stream, void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+    void *p = nullptr;
+    // In host code the array's name is only a stand-in; the runtime maps it
+    // to this device's copy.
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        // In host code the array's name is only a stand-in; the runtime maps
-        // it to this device's copy.
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
+    if (g_scratch_ptr[dev] != p) {
         if (cudaMemsetAsync(p, 0, dsa::kStatusBytes, stream) != cudaSuccess) return DSA_ERR_CUDA;
         g_scratch_ptr[dev] = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return DSA_OK;
 }
 
