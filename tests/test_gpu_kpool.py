@@ -145,6 +145,15 @@ def test_kpool_decode_glm53_flash_shape(dsa):
     assert g.shape == (5, 2051)
 
 
+def test_kpool_long_rows_balanced_grid(dsa):
+    """Rows of up to 30000 pools: the decode score grid shares its CTAs out
+    by sequence length in pool mode; a sequence with no complete pool gets
+    no CTA and an empty row (tail only)."""
+    wl = _decode_wl("kp_long", 97, [120001, 40002, 3], H_I=32, H=8, top_k=2048)
+    g = _run_decode(dsa, wl, 2048)
+    assert g[2].tolist()[:3] == [0, 1, 2] and all(x == -1 for x in g[2].tolist()[3:])
+
+
 def test_kpool_short_sequences_and_small_top_k(dsa):
     """Tokens with no complete pool (tail only), fewer pools than selected,
     and top_k below one pool's worth (tail only)."""
