@@ -18,9 +18,10 @@
 // one key row (its TMEM lane) and reduces sum_h w * max(0, D) for each of its
 // tokens in registers -- no cross-thread reduction.
 //
-// Warp roles: warp 0 issues TMA loads (4-stage ring of 32 KB key tiles),
-// warp 1 allocates TMEM and issues MMAs, warps 2..5 stage the queries and run
-// the epilogue.  All waits are bounded (1 s) and end in DSA_DEV_TIMEOUT.
+// Warp roles: warp 0 issues TMA loads (a ring of 2-4 32 KB key tiles),
+// warp 1 allocates TMEM and issues MMAs, the 4 or 16 warps after them stage
+// the queries and run the epilogue.  All waits are bounded (1 s by default)
+// and end in DSA_DEV_TIMEOUT.
 #include <algorithm>
 
 #include "dsa_common.cuh"
