@@ -633,10 +633,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge split partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const uint16_t *__restrict__ part_o,
-                                                           const float *__restrict__ part_ml,
-                                                           int n_split, int H, int groups, float *out, float *lse,
-                                                           unsigned long long *timeline) {
+// NF partial rows are loaded at a time.  With NF = 4 (up to four splits)
+// the kernel fits in 32 registers, so 16 CTAs share an SM and a grid of
+// thousands of (token, head) CTAs runs in one wave; NF = 16 keeps five CTAs
+// per SM.
+template <int NF>
+__global__ void __launch_bounds__(128, NF <= 4 ? 16 : 5) attn_combine_kernel(const uint16_t *__restrict__ part_o,
+                                                                            const float *__restrict__ part_ml,
+                                                                            int n_split, int H, int groups,
+                                                                            float *out, float *lse,
+                                                                            unsigned long long *timeline) {
     __shared__ float wgt[128];
     __shared__ float ml[2][128];
     const int t = blockIdx.x, h = blockIdx.y;
@@ -661,14 +667,14 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const uint16_t *__res
     }
     __syncthreads();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < n_split; s0 += 16) {              // 16 loads in flight
-        uint2 o[16];
+    for (int s0 = 0; s0 < n_split; s0 += NF) {              // NF loads in flight
+        uint2 o[NF];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
+        for (int u = 0; u < NF; ++u)
             if (s0 + u < n_split)
                 o[u] = __ldg(reinterpret_cast<const uint2 *>(part_o + (base + (s0 + u) * stride) * D_L) + threadIdx.x);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < NF; ++u) {
             if (s0 + u < n_split) {
                 const float w = wgt[s0 + u];
                 const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&o[u].x));
@@ -727,7 +733,10 @@ cudaError_t launch_attn_combine(const AttnLaunch &a, const DevBatch &b, cudaStre
     if (a.n_split > 128) return cudaErrorInvalidConfiguration;
     const int groups = (a.H + kHeads - 1) / kHeads;
     dim3 grid((unsigned)b.T, (unsigned)a.H);
-    return launch_k(attn_combine_kernel, grid, dim3(128), 0, stream, pdl, (const uint16_t *)a.part_o,
+    if (a.n_split <= 4)
+        return launch_k(attn_combine_kernel<4>, grid, dim3(128), 0, stream, pdl, (const uint16_t *)a.part_o,
+                        (const float *)a.part_ml, a.n_split, a.H, groups, a.out, a.lse, b.timeline);
+    return launch_k(attn_combine_kernel<16>, grid, dim3(128), 0, stream, pdl, (const uint16_t *)a.part_o,
                     (const float *)a.part_ml, a.n_split, a.H, groups, a.out, a.lse, b.timeline);
 }
 
