@@ -523,23 +523,15 @@ __global__ void __launch_bounds__(ScoreCfg<kEpi>::kThreads, kEpi >= 8 ? 1 : 2)
                         sm.new_key[c];
                 fence_proxy_async_smem();
             };
-            if constexpr (kEpi == 4) {
-                // Decode CTAs run one or two tiles, so the issue path would
-                // first be fetched into the instruction cache when the first
-                // tile has landed (measured on GB300 after an L2 flush: 2.2 us
-                // from tile to issued products, 0.5 us for the second tile).
-                // Issue it once now on whatever the buffers hold: the first
-                // product of the real step does not accumulate, so it
-                // overwrites this result, and nothing reads the accumulator
-                // before that step's commit.
-            }
             if (!wait_bar(smem_u32(&sm.q_ready), 0, sm, p.status, b.wait_ns)) {
                 // the loops below are skipped
             } else if constexpr (kEpi == 4) {
                 tc_fence_after();
                 // one token: one step per tile, the stage released before the
                 // accumulator is signalled (measured on GB300, ragged
-                // long-context decode: 7 us per step faster than the general loop)
+                // long-context decode: 7 us per step faster than the general
+                // loop; issuing the step from a rolled loop over its K slices
+                // was slower by 0.4 us)
                 for (int i = 0; i < n_mma; ++i) {
                     const int s = i % n_stages;
                     const uint32_t k = (uint32_t)(i / n_stages);
