@@ -59,6 +59,11 @@ CASES = [
                                      cu_q=[0, 1, 2, 3], H_I=16, H=16, top_k=256)),
     ("decode_bs256", 256, S.Workload("paged", 93, kv_len=[4100, 300], q_pos=[4099, 299], cu_q=[0, 1, 2],
                                      H_I=32, H=64, top_k=2048, hadamard=True)),
+    # 40 sequences selecting 2048 of 2100-4000 keys: the attention splits
+    # each token over few CTAs of many tiles, which prefetch their next
+    # tile's (paged) rows into L2
+    ("decode_many_bs64", 64, S.decode_workload("paged_many", 95, S.ragged_lengths(95, 40, lo=2100, hi=4000),
+                                              H_I=16, H=16, top_k=2048)),
     ("chunks_bs64", 64, S.Workload("paged", 94, kv_len=[700, 3000],
                                    q_pos=[680 + i for i in range(20)] + [2990 + i for i in range(10)],
                                    cu_q=[0, 20, 30], H_I=64, H=64, top_k=512, hadamard=True)),
